@@ -1,0 +1,221 @@
+"""Explicit ring simulation of reduce-scatter, all-gather and all-reduce
+(oracle; test infrastructure).
+
+K simulated ranks each hold a buffer of N elements split into K equal chunks of
+S = N / K (chunk c = elements [c*S, (c+1)*S)).  The ring is rank r -> rank
+(r + 1) mod K.  Each round, every rank copies one chunk into a message for its
+right neighbour; then every receiver applies the message it got.
+
+Reduce-scatter (K - 1 rounds).  In round i = 0 .. K-2 rank r sends chunk
+(r - i) mod K and the receiver adds the message to its own copy of that chunk.
+After K - 1 rounds rank r holds the complete sum of chunk (r + 1) mod K.
+  - CMU 11-868 Lecture 14 notes, section 3.2 (ring all-reduce): the send index
+    (r - i) mod K, the landing rule, and the MPI loop's receive index
+    (r - i - 1) mod K.
+  - Ring All-Reduce illustrated (CSDN), Phase 1 Rounds 1.1-1.3: chunk j leaves
+    GPU j, collects one addend per hop for K - 1 hops, lands on GPU (j-1) mod K.
+So the partial sum of chunk j, element t, is built in ring order
+  ((x_j + x_{j+1}) + x_{j+2}) + ... + x_{j-1}     (indices mod K)
+and, the pages' systems being ZeRO, the landed sum of chunk j is written to
+partition slot j (DeepSpeed ZeRO-3 source walkthrough, section 5.2: rank r
+keeps flat[r*chunk : (r+1)*chunk]).
+
+All-gather (K - 1 rounds).  A rank that holds complete chunk (r + d) mod K sends,
+in round i, chunk (r + d - i) mod K; the receiver overwrites its copy (no add).
+After the reduce-scatter d = 1 (lecture section 3.2, send index (r + 1 - i)
+mod K; CSDN Phase 2); for a parameter all-gather from ZeRO shards, rank r starts
+with its own shard r, so d = 0.
+
+Summation modes.
+  RING_FP32: rank copies and messages are fp32; each hop is one fp32 add,
+             round to nearest even.
+  HOP_BF16:  rank copies and messages are bf16 (bf16 on the wire, as in the
+             "bf16 communication" setting of DeepSpeed issue 8364); each hop
+             rounds the fp32 sum back to bf16.
+Averaging: the landed sum is multiplied once by an fp32 `scale` (1/K for the
+average: sum, then divide by the world size -- lecture section 4.1).
+Micro-batches: with M > 1 micro-batches per rank, each rank first accumulates
+its own bf16 gradients, g = bf16(g0 + g1 + ...), left to right, before the ring
+(lecture section 4.2, gradient accumulation before the all-reduce).
+Accumulate: with `accumulate`, the scaled shard is added to the existing fp32
+partition gradient instead of replacing it (ZeRO-3 walkthrough, section 5.3:
+copy_ on the first micro step, add_ afterwards) -- one fp32 multiply, then one
+fp32 add, two roundings.
+All-reduce = reduce-scatter + all-gather (lecture section 2.2): the landing
+rank multiplies its complete chunk by `scale`, rounds it to bf16, and the
+all-gather circulates the bf16 result.
+
+Traffic.  Every round each rank sends exactly one chunk, so after a full
+all-reduce each rank has sent 2(K - 1) * S = 2(K - 1) N / K elements in
+2(K - 1) rounds (lecture section 3.2 and exercise 4; CSDN summary).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import bf16
+
+RING_FP32 = 0
+HOP_BF16 = 1
+
+
+@dataclass
+class Counters:
+    K: int
+    rounds: int = 0
+    sent: list = field(default_factory=list)      # elements sent, per rank
+
+    def __post_init__(self):
+        if not self.sent:
+            self.sent = [0] * self.K
+
+
+@dataclass
+class Trace:
+    """Round-by-round record: for each round, the sends (sender, receiver,
+    chunk) and a copy of every rank's buffer after the round."""
+    rounds: list = field(default_factory=list)    # (phase, i, sends, [state copies])
+
+
+def _chunk(a: np.ndarray, c: int, S: int) -> np.ndarray:
+    return a[c * S:(c + 1) * S]
+
+
+def _check(K: int, N: int):
+    if K < 2:
+        raise ValueError("a ring needs K >= 2 ranks")
+    if N <= 0 or N % K:
+        raise ValueError("N must be a positive multiple of K (equal chunks)")
+
+
+def local_accumulate(micro_bufs: list) -> np.ndarray:
+    """g = bf16(...(bf16(g0 + g1) + g2)...): rank-local gradient accumulation."""
+    g = np.asarray(micro_bufs[0], dtype=np.uint16).copy()
+    for m in micro_bufs[1:]:
+        g = bf16.add(g, np.asarray(m, dtype=np.uint16))
+    return g
+
+
+def _rs_rounds(state: list, K: int, S: int, mode: int, ctr: Counters, trace: Trace | None):
+    for i in range(K - 1):
+        # every rank puts one chunk on its outgoing link ...
+        msgs = []
+        for r in range(K):
+            c = (r - i) % K
+            msgs.append((r, (r + 1) % K, c, _chunk(state[r], c, S).copy()))
+        # ... then every receiver reduces what arrived into its own copy
+        for src, dst, c, msg in msgs:
+            mine = _chunk(state[dst], c, S)
+            if mode == RING_FP32:
+                with np.errstate(over="ignore", invalid="ignore"):
+                    mine[:] = mine + msg
+            else:
+                mine[:] = bf16.add(mine, msg)
+            ctr.sent[src] += S
+        ctr.rounds += 1
+        if trace is not None:
+            trace.rounds.append(("rs", i, [(s, d, c) for s, d, c, _ in msgs],
+                                 [a.copy() for a in state]))
+
+
+def _ag_rounds(state: list, K: int, S: int, d: int, ctr: Counters, trace: Trace | None):
+    for i in range(K - 1):
+        msgs = []
+        for r in range(K):
+            c = (r + d - i) % K
+            msgs.append((r, (r + 1) % K, c, _chunk(state[r], c, S).copy()))
+        for src, dst, c, msg in msgs:
+            _chunk(state[dst], c, S)[:] = msg          # overwrite, no reduction
+            ctr.sent[src] += S
+        ctr.rounds += 1
+        if trace is not None:
+            trace.rounds.append(("ag", i, [(s, d_, c) for s, d_, c, _ in msgs],
+                                 [a.copy() for a in state]))
+
+
+def _initial_state(x: list, K: int, M: int, mode: int) -> list:
+    if len(x) != M * K:
+        raise ValueError("expected M*K input buffers, x[m*K + r]")
+    g = [local_accumulate([x[m * K + r] for m in range(M)]) for r in range(K)]
+    if mode == RING_FP32:
+        return [bf16.to_f32(gr).copy() for gr in g]
+    if mode == HOP_BF16:
+        return g
+    raise ValueError("mode must be RING_FP32 or HOP_BF16")
+
+
+def _landed_f32(state: list, K: int, S: int, j: int, mode: int) -> np.ndarray:
+    """Complete sum of chunk j, read from the rank it landed on, (j - 1) mod K."""
+    v = _chunk(state[(j - 1) % K], j, S)
+    return v.astype(np.float32) if mode == RING_FP32 else bf16.to_f32(v)
+
+
+def reduce_scatter(x: list, K: int, M: int = 1, mode: int = RING_FP32,
+                   scale: float = 1.0, out_init: list | None = None,
+                   trace: Trace | None = None):
+    """Ring reduce-scatter of K rank buffers (M micro-batches each) into K fp32
+    partition shards.
+
+    x        : list of M*K uint16 arrays (bf16 bits) of equal length N;
+               x[m*K + r] is rank r's gradient of micro-batch m.
+    out_init : None (copy) or K float32 arrays of N/K to accumulate into.
+    Returns (shards, counters): shards[j] = float32 array of N/K, slot j.
+    """
+    N = len(x[0])
+    _check(K, N)
+    S = N // K
+    state = _initial_state(x, K, M, mode)
+    ctr = Counters(K)
+    _rs_rounds(state, K, S, mode, ctr, trace)
+    f_scale = np.float32(scale)
+    shards = []
+    for j in range(K):
+        v = _landed_f32(state, K, S, j, mode) * f_scale
+        if out_init is not None:
+            v = np.asarray(out_init[j], dtype=np.float32) + v
+        shards.append(v.astype(np.float32))
+    return shards, ctr
+
+
+def allgather(shards: list, K: int, trace: Trace | None = None):
+    """Ring all-gather of K bf16 shards (shard j owned by rank j) into K full
+    buffers of N = K*S.  Positions a rank has not received yet hold zeros in
+    the trace.  Returns (outs, counters), outs[r] a uint16 array of N."""
+    S = len(shards[0])
+    if len(shards) != K or any(len(s) != S for s in shards) or S == 0:
+        raise ValueError("need K shards of equal, non-zero length")
+    N = K * S
+    state = []
+    for r in range(K):
+        a = np.zeros(N, dtype=np.uint16)
+        _chunk(a, r, S)[:] = np.asarray(shards[r], dtype=np.uint16)
+        state.append(a)
+    ctr = Counters(K)
+    _ag_rounds(state, K, S, 0, ctr, trace)
+    return state, ctr
+
+
+def allreduce(x: list, K: int, mode: int = RING_FP32, scale: float = 1.0,
+              trace: Trace | None = None):
+    """Ring all-reduce = reduce-scatter + all-gather of K bf16 rank buffers.
+    Returns (outs, counters), outs[r] a uint16 array of N (bf16 bits)."""
+    N = len(x[0])
+    _check(K, N)
+    S = N // K
+    state = _initial_state(list(x), K, 1, mode)
+    ctr = Counters(K)
+    _rs_rounds(state, K, S, mode, ctr, trace)
+    # the landing rank scales its complete chunk and rounds it to bf16; the
+    # rest of its buffer holds stale partial sums that the all-gather overwrites
+    f_scale = np.float32(scale)
+    wire = []
+    for r in range(K):
+        a = state[r]
+        w = bf16.from_f32(a) if mode == RING_FP32 else a.copy()
+        c = (r + 1) % K
+        _chunk(w, c, S)[:] = bf16.from_f32(_landed_f32(state, K, S, c, mode) * f_scale)
+        wire.append(w)
+    _ag_rounds(wire, K, S, 1, ctr, trace)
+    return wire, ctr
