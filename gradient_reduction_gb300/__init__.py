@@ -1,0 +1,25 @@
+"""ZeRO gradient-bucket reduction on one GB300 GPU (sm_103a).
+
+K data-parallel ranks are simulated as K buffers in one GPU's memory.  The
+library libdpr (C ABI in include/dpr.h, CUDA kernels in csrc/) provides the
+flat-bucket gather of fragmented gradients, the ring-order reduce-scatter
+with averaging and the fp32 partition cast, the all-gather and the fused
+all-reduce.  This package is the thin Python binding of those calls.
+"""
+from ._binding import (  # noqa: F401
+    HOP_BF16,
+    LIB_PATH,
+    RING_FP32,
+    DprError,
+    FlattenPlan,
+    dpr_allgather,
+    dpr_allreduce,
+    dpr_bucket_assign,
+    dpr_flatten_bucket,
+    dpr_flatten_plan_create,
+    dpr_flatten_plan_destroy,
+    dpr_reduce_scatter,
+    dpr_strerror,
+    dpr_version,
+    lib,
+)

@@ -1,0 +1,216 @@
+"""ctypes binding of libdpr (include/dpr.h), with the same entry-point names.
+
+Argument marshalling only: tensors are turned into device pointers and sizes,
+the current CUDA stream is passed along, and a non-zero status becomes a
+DprError.  The checks here (dtype, device, contiguity, element counts) exist
+so that a wrongly sized tensor is rejected on the host instead of being read
+out of bounds on the GPU.  Every step of the computation runs in libdpr's
+kernels; there is no other implementation to fall back to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+import torch
+
+RING_FP32 = 0
+HOP_BF16 = 1
+_MODES = {"ring_fp32": RING_FP32, "hop_bf16": HOP_BF16, RING_FP32: RING_FP32, HOP_BF16: HOP_BF16}
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libdpr.so")
+
+_c_p = ctypes.c_void_p
+_pp = ctypes.POINTER(ctypes.c_void_p)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_SIGS = {
+    "dpr_reduce_scatter": [_pp, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _pp, ctypes.c_int,
+                           ctypes.c_float, ctypes.c_int, _c_p],
+    "dpr_allgather": [_pp, ctypes.c_int, ctypes.c_int64, _pp, _c_p],
+    "dpr_allreduce": [_pp, ctypes.c_int, ctypes.c_int64, _pp, ctypes.c_int, ctypes.c_float, _c_p],
+    "dpr_flatten_plan_create": [ctypes.POINTER(_c_p), ctypes.c_int, ctypes.c_int, _pp, _i64p,
+                                _i64p, ctypes.c_int64, _c_p],
+    "dpr_flatten_bucket": [_c_p, _pp, _c_p],
+    "dpr_flatten_plan_destroy": [_c_p],
+    "dpr_bucket_assign": [_i64p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                          ctypes.POINTER(ctypes.c_int32), _i64p, _i64p,
+                          ctypes.POINTER(ctypes.c_int)],
+    "dpr_strerror": [ctypes.c_int],
+    "dpr_last_cuda_error": [],
+    "dpr_version": [],
+}
+_RESTYPES = {"dpr_strerror": ctypes.c_char_p, "dpr_version": ctypes.c_char_p}
+
+_lib = None
+
+
+class DprError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = lib().dpr_strerror(status).decode()
+        if status == 4:
+            msg += f" (cudaError {lib().dpr_last_cuda_error()})"
+        super().__init__(f"{fn}: {msg} [status {status}]")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libdpr; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libdpr is not built ({LIB_PATH} missing): run "
+                "`python -m gradient_reduction_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = _RESTYPES.get(name, ctypes.c_int)
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise DprError(fn, status)
+
+
+def _ptrs(ts: Sequence[torch.Tensor]):
+    return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _need(ts: Sequence[torch.Tensor], count: int, dtype, n: int, what: str):
+    if len(ts) != count:
+        raise ValueError(f"{what}: expected {count} tensors, got {len(ts)}")
+    for t in ts:
+        if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+            raise ValueError(f"{what}: need contiguous CUDA {dtype} tensors")
+        if t.numel() < n:
+            raise ValueError(f"{what}: tensor of {t.numel()} elements, need {n}")
+
+
+def dpr_reduce_scatter(inputs: Sequence[torch.Tensor], K: int, M: int, N: int,
+                       outputs: Sequence[torch.Tensor], mode=RING_FP32, scale: float | None = None,
+                       accumulate: bool = False, stream=None) -> None:
+    """inputs[m*K + r]: bf16 (N,), rank r micro-batch m; outputs[j]: fp32 (N/K,)."""
+    if N > 0:
+        _need(inputs, M * K, torch.bfloat16, N, "inputs")
+        _need(outputs, K, torch.float32, N // K if K else 0, "outputs")
+    st = lib().dpr_reduce_scatter(_ptrs(inputs), K, M, N, _ptrs(outputs), _MODES[mode],
+                                  1.0 / K if scale is None else scale, int(bool(accumulate)),
+                                  _stream(stream))
+    _check("dpr_reduce_scatter", st)
+
+
+def dpr_allgather(shards: Sequence[torch.Tensor], K: int, N: int,
+                  outputs: Sequence[torch.Tensor], stream=None) -> None:
+    """shards[j]: bf16 (N/K,); outputs[r]: bf16 (N,)."""
+    if N > 0:
+        _need(shards, K, torch.bfloat16, N // K if K else 0, "shards")
+        _need(outputs, K, torch.bfloat16, N, "outputs")
+    _check("dpr_allgather", lib().dpr_allgather(_ptrs(shards), K, N, _ptrs(outputs),
+                                                _stream(stream)))
+
+
+def dpr_allreduce(inputs: Sequence[torch.Tensor], K: int, N: int,
+                  outputs: Sequence[torch.Tensor], mode=RING_FP32, scale: float | None = None,
+                  stream=None) -> None:
+    """inputs[r], outputs[r]: bf16 (N,); outputs may be the inputs (in place)."""
+    if N > 0:
+        _need(inputs, K, torch.bfloat16, N, "inputs")
+        _need(outputs, K, torch.bfloat16, N, "outputs")
+    st = lib().dpr_allreduce(_ptrs(inputs), K, N, _ptrs(outputs), _MODES[mode],
+                             1.0 / K if scale is None else scale, _stream(stream))
+    _check("dpr_allreduce", st)
+
+
+class FlattenPlan:
+    """Owns a dpr_flatten_plan and keeps its source gradients alive."""
+
+    def __init__(self, handle: int, K: int, bucket_numel: int, srcs: list):
+        self.handle = handle
+        self.K = K
+        self.bucket_numel = bucket_numel
+        self._srcs = srcs
+
+    def close(self):
+        if self.handle:
+            h, self.handle = self.handle, None
+            _check("dpr_flatten_plan_destroy", lib().dpr_flatten_plan_destroy(h))
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dpr_flatten_plan_create(srcs: Sequence[Sequence[torch.Tensor]], numel: Sequence[int],
+                            offset: Sequence[int], bucket_numel: int, stream=None) -> FlattenPlan:
+    """srcs[r][p]: rank r's gradient p (bf16, numel[p] elements, any shape)."""
+    K = len(srcs)
+    P = len(numel)
+    flat = []
+    for r in range(K):
+        if len(srcs[r]) != P:
+            raise ValueError("every rank needs P gradients")
+        for p in range(P):
+            t = srcs[r][p]
+            if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError("gradients must be contiguous CUDA bf16 tensors")
+            if t.numel() != numel[p]:
+                raise ValueError(f"gradient {p} of rank {r}: {t.numel()} elements, numel says {numel[p]}")
+            flat.append(t)
+    h = ctypes.c_void_p()
+    n_arr = (ctypes.c_int64 * P)(*numel)
+    o_arr = (ctypes.c_int64 * P)(*offset)
+    st = lib().dpr_flatten_plan_create(ctypes.byref(h), K, P, _ptrs(flat), n_arr, o_arr,
+                                       bucket_numel, _stream(stream))
+    _check("dpr_flatten_plan_create", st)
+    return FlattenPlan(h.value, K, bucket_numel, flat)
+
+
+def dpr_flatten_bucket(plan: FlattenPlan, dst: Sequence[torch.Tensor], stream=None) -> None:
+    """dst[r]: rank r's flat bucket, bf16 (bucket_numel,)."""
+    _need(dst, plan.K, torch.bfloat16, plan.bucket_numel, "dst")
+    _check("dpr_flatten_bucket", lib().dpr_flatten_bucket(plan.handle, _ptrs(dst), _stream(stream)))
+
+
+def dpr_flatten_plan_destroy(plan: FlattenPlan) -> None:
+    plan.close()
+
+
+def dpr_bucket_assign(numel: Sequence[int], cap: int, pad_to: int = 1):
+    """Returns (bucket_of[P], offset[P], bucket_numel[n_buckets])."""
+    P = len(numel)
+    n_arr = (ctypes.c_int64 * max(P, 1))(*numel)
+    b_of = (ctypes.c_int32 * max(P, 1))()
+    off = (ctypes.c_int64 * max(P, 1))()
+    bn = (ctypes.c_int64 * max(P, 1))()
+    nb = ctypes.c_int()
+    st = lib().dpr_bucket_assign(n_arr, P, cap, pad_to, b_of, off, bn, ctypes.byref(nb))
+    _check("dpr_bucket_assign", st)
+    return list(b_of[:P]), list(off[:P]), list(bn[:nb.value])
+
+
+def dpr_strerror(status: int) -> str:
+    return lib().dpr_strerror(status).decode()
+
+
+def dpr_version() -> str:
+    return lib().dpr_version().decode()

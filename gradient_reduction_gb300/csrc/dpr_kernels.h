@@ -1,0 +1,75 @@
+// Kernel parameter blocks and host-side launchers of libdpr (internal).
+//
+// Every parameter block is passed to its kernel by value as a
+// __grid_constant__ argument, so a launch needs no device-side table of
+// pointers and allocates nothing.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/dpr.h"
+
+namespace dpr {
+
+constexpr int kThreads = 256;      // threads per block of every kernel
+
+struct RsParams {
+    const uint16_t* in[DPR_MAX_MICRO * DPR_MAX_RANKS];  // in[m*K + r]
+    float* out[DPR_MAX_RANKS];                          // partition shard j
+    int64_t S;          // elements per chunk
+    uint32_t su;        // 8-element units per chunk (vector kernels)
+    int K;
+    int M;
+    float scale;
+    int accumulate;
+};
+
+struct ArParams {
+    const uint16_t* in[DPR_MAX_RANKS];
+    uint16_t* out[DPR_MAX_RANKS];
+    int64_t S;
+    uint32_t su;
+    int K;
+    float scale;
+};
+
+struct AgParams {
+    const uint16_t* shard[DPR_MAX_RANKS];
+    uint16_t* out[DPR_MAX_RANKS];
+    int64_t S;
+    uint32_t su;
+    int K;
+};
+
+// One gradient of one rank inside a flatten plan.
+struct FlatSeg {
+    const uint16_t* src;
+    int64_t dst_off;    // element offset inside the rank's flat bucket
+    int64_t numel;
+    int64_t tile0;      // index of this segment's first tile in the plan
+    int32_t rank;
+    int32_t pad;
+};
+
+struct FlatParams {
+    const FlatSeg* segs;
+    int64_t n_seg;
+    int64_t n_tiles;
+    uint16_t* dst[DPR_MAX_RANKS];
+};
+
+constexpr int64_t kFlatTile = 8192;     // elements per flatten tile (16 KB)
+
+// Launchers: return cudaSuccess or the launch error.  `vec` selects the
+// 16-byte kernels (all buffers 16-byte aligned and S % 8 == 0).
+cudaError_t launch_reduce_scatter(const RsParams& p, int mode, bool vec, cudaStream_t s);
+cudaError_t launch_allreduce(const ArParams& p, int mode, bool vec, cudaStream_t s);
+cudaError_t launch_allgather(const AgParams& p, bool vec, cudaStream_t s);
+cudaError_t launch_flatten(const FlatParams& p, cudaStream_t s);
+
+// Grid helper: blocks per chunk so that K chunks together fill the GPU with
+// `blocks_per_sm` resident blocks per SM, and no more blocks than there is work.
+cudaError_t blocks_per_chunk(const void* kernel, int K, uint64_t work_per_chunk, int* gx);
+
+}  // namespace dpr

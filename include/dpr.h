@@ -1,0 +1,187 @@
+/*
+ * dpr.h -- C ABI of libdpr: the data-parallel gradient-bucket reduction of
+ * ZeRO, with the K data-parallel ranks simulated as K buffers in the memory
+ * of one GPU (sm_103a).
+ *
+ * Conventions shared by every call (after the NCCL call shape described in
+ * CMU 11-868 Lecture 14 notes, section 2.3: send/receive buffers, an element
+ * count, the reduction, and a CUDA stream):
+ *   - every buffer pointer is a DEVICE pointer owned by the caller; pointer
+ *     ARRAYS (in, out, shard, src, dst) are HOST arrays of such pointers and
+ *     are read during the call only;
+ *   - bf16 buffers are 16-bit IEEE bfloat16 bit patterns, 2-byte aligned;
+ *     fp32 buffers are 4-byte aligned.  Buffers that are all 16-byte aligned
+ *     with 8-element-aligned chunks take the vectorised kernels; any other
+ *     layout takes an element-wise kernel with the same results;
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream); work is
+ *     enqueued asynchronously, nothing synchronises, and completion (and any
+ *     asynchronous execution error) is observed by synchronising the stream;
+ *   - the reduce-scatter, all-gather and all-reduce calls allocate nothing
+ *     and launch exactly one kernel; N == 0 is a no-op that launches nothing;
+ *   - arguments are validated on the host before anything is launched; a
+ *     rejected call returns its status and has no effect.  DPR_ERR_CUDA
+ *     means a CUDA call failed; dpr_last_cuda_error() then returns its
+ *     cudaError_t (per calling thread).
+ *
+ * Chunks: a rank buffer of N elements is cut into K equal chunks of S = N/K,
+ * chunk j = elements [j*S, (j+1)*S).  N must be a multiple of K.
+ */
+#ifndef DPR_H
+#define DPR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dpr_status {
+    DPR_OK = 0,
+    DPR_ERR_INVALID_ARG = 1, /* null pointer, K/M/N out of range, N % K != 0, bad mode */
+    DPR_ERR_ALIGNMENT = 2,   /* a bf16 pointer not 2-byte / fp32 pointer not 4-byte aligned */
+    DPR_ERR_UNSUPPORTED = 3, /* a size beyond the documented limits */
+    DPR_ERR_CUDA = 4,        /* a CUDA call failed; see dpr_last_cuda_error() */
+    DPR_ERR_ALIAS = 5        /* outputs overlap inputs or each other (beyond allowed in-place forms) */
+} dpr_status;
+
+typedef enum dpr_sum_mode {
+    /* fp32 partial sums: each hop is one fp32 add, round to nearest even */
+    DPR_SUM_RING_FP32 = 0,
+    /* bf16 partial sums on the wire: each hop's fp32 sum is rounded back to bf16 */
+    DPR_SUM_HOP_BF16 = 1
+} dpr_sum_mode;
+
+#define DPR_MAX_RANKS 64                 /* 2 <= K <= 64 */
+#define DPR_MAX_MICRO 2                  /* 1 <= M <= 2 */
+#define DPR_MAX_ELEMS (((int64_t)1) << 34) /* N per rank buffer */
+
+/*
+ * Ring reduce-scatter with averaging and the fp32 partition-gradient cast.
+ *
+ * Defines: CMU 11-868 Lecture 14 notes, section 3.2 (ring reduce-scatter:
+ * in round i rank r sends chunk (r - i) mod K, the receiver adds it; after
+ * K-1 rounds rank r holds the complete chunk (r + 1) mod K) and "Ring
+ * All-Reduce illustrated" (CSDN), Phase 1: chunk j starts at rank j and
+ * collects ranks j+1, ..., j-1.  The result is therefore, per element t of
+ * chunk j, the sum in ring order
+ *     acc = ((x_j[t] + x_{j+1}[t]) + x_{j+2}[t]) + ... + x_{j-1}[t]
+ * (indices mod K; in DPR_SUM_HOP_BF16 every partial sum is rounded to bf16).
+ * With M = 2, each rank's input is first its local accumulation
+ * x_r = bf16(g0_r + g1_r) (lecture section 4.2, accumulate before reduce).
+ * The landed sum is averaged and cast to fp32 into partition slot j
+ * (DeepSpeed ZeRO-3 source walkthrough, sections 1, 5.2, 5.3 and 8):
+ *     accumulate == 0:  out[j][t] = fp32(acc) * scale          (copy_)
+ *     accumulate != 0:  out[j][t] = out[j][t] + fp32(acc)*scale (add_)
+ * with the multiply and the add each rounded (no fused multiply-add).
+ *
+ *   in    host array [M*K]; in[m*K + r] = rank r's micro-batch m gradient,
+ *         bf16, N elements.  Input buffers may overlap each other.
+ *   K     ranks, 2..64;   M  micro-batches, 1..2;   N  elements per rank.
+ *   out   host array [K]; out[j] = partition shard j, fp32, N/K elements.
+ *         Shards must not overlap each other or any input.
+ *   mode  dpr_sum_mode;   scale  fp32 multiplier (1.0f/K averages).
+ */
+dpr_status dpr_reduce_scatter(const void* const* in, int K, int M, int64_t N,
+                              float* const* out, int mode, float scale, int accumulate,
+                              void* stream);
+
+/*
+ * Ring all-gather of K shards into K full replicas.
+ *
+ * Defines: lecture section 3.2 and CSDN Phase 2 (complete chunks travel the
+ * ring and overwrite, so every rank ends with all K chunks); the ZeRO-3
+ * parameter all-gather that rebuilds full parameters from 1/K shards
+ * (DeepSpeed ZeRO-3 source walkthrough, sections 1 and 2.1):
+ *     out[r][j*S + t] = shard[j][t]   for every r, j, t   (a bit copy)
+ *
+ *   shard  host array [K]; shard[j] = bf16, S = N/K elements.
+ *   out    host array [K]; out[r] = bf16, N elements.  Outputs must not
+ *          overlap each other or any shard, except the in-place form
+ *          shard[j] == out[j] + j*S (rank j's shard lives inside its own
+ *          full buffer).
+ */
+dpr_status dpr_allgather(const void* const* shard, int K, int64_t N, void* const* out,
+                         void* stream);
+
+/*
+ * Ring all-reduce = reduce-scatter + all-gather (lecture section 2.2), fused
+ * into one pass: each element's ring-order sum (as in dpr_reduce_scatter,
+ * M = 1) is multiplied by scale, rounded once to bf16, and written to every
+ * replica, so all K outputs are bitwise identical (CSDN, end of Phase 2):
+ *     out[r][t] = bf16(fp32(acc) * scale)   for every r
+ * This is the contiguous-gradient path of ZeRO-3 (DeepSpeed ZeRO-3 source
+ * walkthrough, section 5.2: all-reduce the flat bucket, then slice).
+ *
+ *   in   host array [K], bf16, N elements each.
+ *   out  host array [K], bf16, N elements each; out[r] == in[r] (in place)
+ *        is allowed, any other overlap is rejected.
+ */
+dpr_status dpr_allreduce(const void* const* in, int K, int64_t N, void* const* out, int mode,
+                         float scale, void* stream);
+
+/*
+ * Flat-bucket gather plan (the IPG bucket of ZeRO: DeepSpeed ZeRO-3 source
+ * walkthrough, sections 3.2 and 5.1).  Gradient p of rank r occupies
+ * elements [offset[p], offset[p] + numel[p]) of rank r's flat bucket.  In the
+ * pages' system the gradient is written there directly; here the per-rank
+ * gradients already exist as separate buffers, so flattening is a copy.
+ *
+ * dpr_flatten_plan_create records the table once (offsets are fixed after
+ * initialisation): it allocates a device copy of it (the only allocation in
+ * this library), uploads it on `stream` and waits for the upload, so the plan
+ * can then be used on any stream.
+ *   src          host array [K*P]; src[r*P + p] = rank r's gradient p, bf16.
+ *   numel, offset host arrays [P], elements; spans must lie inside
+ *                [0, bucket_numel) and not overlap.  numel[p] == 0 is allowed.
+ *   *plan        receives the plan (NULL on failure).
+ */
+typedef struct dpr_flatten_plan dpr_flatten_plan;
+
+dpr_status dpr_flatten_plan_create(dpr_flatten_plan** plan, int K, int P, const void* const* src,
+                                   const int64_t* numel, const int64_t* offset,
+                                   int64_t bucket_numel, void* stream);
+
+/*
+ * Executes a plan: one kernel copies every gradient of every rank into the
+ * flat buckets, dst[r][offset[p] + t] = src[r*P + p][t] (a bit copy).
+ * Positions no gradient covers (padding) are not written.
+ *   dst  host array [K]; dst[r] = rank r's flat bucket, bf16, bucket_numel
+ *        elements; must not overlap each other or any source gradient.
+ * The plan must stay alive until the copy has completed on the stream.
+ */
+dpr_status dpr_flatten_bucket(const dpr_flatten_plan* plan, void* const* dst, void* stream);
+
+/* Frees a plan (its device table); synchronises the device.  NULL is a no-op. */
+dpr_status dpr_flatten_plan_destroy(dpr_flatten_plan* plan);
+
+/*
+ * Bucket formation, host only (DeepSpeed ZeRO-3 source walkthrough, sections
+ * 3.1, 5.1, 5.4): gradients in arrival order are appended at the running
+ * offset; the bucket is flushed first when adding the next gradient would
+ * take it past `cap` elements; a gradient larger than `cap` forms its own
+ * bucket; the last, partly filled bucket is flushed at the end.  Each
+ * bucket's size is rounded up to a multiple of `pad_to` (K, for equal
+ * chunks); the padding is never written by dpr_flatten_bucket.
+ *   numel        [P] gradient sizes in arrival order (each >= 1)
+ *   bucket_of    [P] out: bucket index of each gradient
+ *   offset       [P] out: element offset of each gradient in its bucket
+ *   bucket_numel [P] out: padded size of each bucket (first *n_buckets used)
+ */
+dpr_status dpr_bucket_assign(const int64_t* numel, int P, int64_t cap, int64_t pad_to,
+                             int32_t* bucket_of, int64_t* offset, int64_t* bucket_numel,
+                             int* n_buckets);
+
+/* Static description of a status code. */
+const char* dpr_strerror(int status);
+
+/* cudaError_t of the calling thread's last DPR_ERR_CUDA (0 if none). */
+int dpr_last_cuda_error(void);
+
+/* Library version string. */
+const char* dpr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DPR_H */

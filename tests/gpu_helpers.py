@@ -1,0 +1,132 @@
+"""Shared pieces of the GPU parity tests: device buffers from the seeded
+generator, and the oracle evaluated on sampled element positions.
+
+A reduce-scatter's result at position t of chunk j depends only on the K (x M)
+inputs at element j*S + t and on j (which fixes the ring order).  So the
+oracle can be run on a sub-problem made of the same positions T of every
+chunk (N' = K*|T| per rank): its shard j is the full problem's shard j at T.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import bf16 as obf
+from oracle import ring
+from workloads import synthetic as syn
+
+MODES = (ring.RING_FP32, ring.HOP_BF16)
+
+
+def device():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    from gradient_reduction_gb300 import build
+    build.build()
+    return torch.device("cuda", 0)
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return syn.bf16_bits(t)
+
+
+def f32_bits(t) -> np.ndarray:
+    a = t.detach().cpu().numpy() if isinstance(t, torch.Tensor) else np.asarray(t)
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+def assert_f32_equal(got, want, what=""):
+    """Bit equality, except that any NaN matches any NaN (payloads differ
+    between the GPU's and the oracle's canonical NaN)."""
+    g, w = np.asarray(got, np.float32), np.asarray(want, np.float32)
+    assert g.shape == w.shape, what
+    nan = np.isnan(w)
+    assert np.array_equal(np.isnan(g), nan), f"{what}: NaN positions differ"
+    ok = f32_bits(g)[~nan] == f32_bits(w)[~nan]
+    if not ok.all():
+        i = int(np.flatnonzero(~ok)[0])
+        raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.size} differ; first at "
+                             f"{i}: got {g[~nan][i]!r} want {w[~nan][i]!r}")
+
+
+def assert_bf16_equal(got_bits, want_bits, what=""):
+    g, w = np.asarray(got_bits, np.uint16), np.asarray(want_bits, np.uint16)
+    assert g.shape == w.shape, what
+    gn = (g & 0x7FFF) > 0x7F80
+    wn = (w & 0x7FFF) > 0x7F80
+    assert np.array_equal(gn, wn), f"{what}: NaN positions differ"
+    ok = g[~wn] == w[~wn]
+    if not ok.all():
+        i = int(np.flatnonzero(~ok)[0])
+        raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.size} differ; first at "
+                             f"{i}: got {hex(g[~wn][i])} want {hex(w[~wn][i])}")
+
+
+def sample_positions(S: int, w: int, seed: int) -> np.ndarray:
+    """Positions inside a chunk: the first and last w, and w random ones."""
+    rng = np.random.default_rng(seed)
+    w = min(w, S)
+    pos = set(range(w)) | set(range(S - w, S))
+    pos |= set(int(x) for x in rng.integers(0, S, w))
+    return np.array(sorted(pos), dtype=np.int64)
+
+
+def gather_positions(get_slab, K: int, S: int, T: np.ndarray) -> np.ndarray:
+    """For one rank buffer: its elements at c*S + T for every chunk c, as bf16
+    bits, concatenated chunk by chunk.  get_slab(start, count) -> bf16 tensor."""
+    parts = []
+    # contiguous runs of T keep the number of generator calls small
+    runs = np.split(T, np.flatnonzero(np.diff(T) != 1) + 1)
+    for c in range(K):
+        for run in runs:
+            parts.append(bits(get_slab(c * S + int(run[0]), len(run))))
+    return np.concatenate(parts)
+
+
+def gather_inputs(slab_fn, K: int, M: int, S: int, T: np.ndarray) -> list:
+    """Host inputs of the sampled sub-problem: x[m*K + r] = rank r's micro m
+    buffer at c*S + T for every chunk c.  slab_fn(rank, micro, start, count)
+    -> bf16 tensor."""
+    return [gather_positions(lambda s, n, r=r, m=m: slab_fn(r, m, s, n), K, S, T)
+            for m in range(M) for r in range(K)]
+
+
+def oracle_rs_sampled(slab_fn, K: int, M: int, S: int, T: np.ndarray, mode: int, scale: float,
+                      out_init=None, x=None):
+    """Oracle reduce-scatter on positions T of every chunk.  Returns K float32
+    arrays of |T|."""
+    if x is None:
+        x = gather_inputs(slab_fn, K, M, S, T)
+    shards, _ = ring.reduce_scatter(x, K, M, mode, scale, out_init=out_init)
+    return shards
+
+
+def oracle_ar_sampled(slab_fn, K: int, S: int, T: np.ndarray, mode: int, scale: float, x=None):
+    if x is None:
+        x = gather_inputs(slab_fn, K, 1, S, T)
+    outs, _ = ring.allreduce(x[:K], K, mode, scale)
+    return outs           # each: K chunks of |T|, chunk by chunk
+
+
+def device_slab_positions(t: torch.Tensor, base: int, T: np.ndarray) -> torch.Tensor:
+    idx = torch.from_numpy(T + base).to(t.device)
+    return t.index_select(0, idx).cpu()
+
+
+def fresh(*shape, dtype, dev, fill=None):
+    t = torch.empty(*shape, dtype=dtype, device=dev)
+    if fill is not None:
+        t.fill_(fill)
+    return t
+
+
+def widen_init(K: int, S: int, key_base: int, dev):
+    """Deterministic fp32 initial partition gradients (for accumulate tests):
+    bf16 generator values widened to fp32 -- identical on host and device."""
+    return [syn.gauss_bf16(0, S, syn.stream_key(key_base, j), 1e-2, device=dev).float()
+            for j in range(K)]
+
+
+def f32_of_bf16_bits(b: np.ndarray) -> np.ndarray:
+    return obf.to_f32(b)

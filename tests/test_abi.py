@@ -1,0 +1,165 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/dpr.h declares, rejects bad arguments on the host before
+anything reaches CUDA, and its host-only bucket formation matches the oracle.
+
+Rejection tests pass fake device addresses: a rejected call returns before
+any CUDA call, so those addresses are never dereferenced."""
+import ctypes
+import os
+import random
+import re
+
+import pytest
+
+from oracle import flatten as ofl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dpr.h")
+
+OK, INVALID, ALIGN, UNSUP, CUDA, ALIAS = range(6)
+
+
+@pytest.fixture(scope="module")
+def L():
+    from gradient_reduction_gb300 import build
+    build.build()
+    import gradient_reduction_gb300 as g
+    return g.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dpr_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(L):
+    names = _declared()
+    assert len(names) == 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_header_is_plain_c():
+    """The header compiles as C (no torch or CUDA types in the signatures)."""
+    import subprocess
+    import tempfile
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "t.c")
+        with open(c, "w") as f:
+            f.write('#include "dpr.h"\nint main(void){return dpr_version()==0;}\n')
+        r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only",
+                            "-I", os.path.join(ROOT, "include"), c], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
+def _arr(vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+BASE = 0x7F0000000000   # fake, 256-byte aligned device addresses; never dereferenced
+
+
+def _bufs(n, size, start=BASE):
+    return [start + i * size for i in range(n)]
+
+
+def test_reduce_scatter_rejections(L):
+    K, N = 4, 64
+    ins, outs = _bufs(K, 1 << 20), _bufs(K, 1 << 20, BASE + (1 << 30))
+    rs = L.dpr_reduce_scatter
+    assert rs(_arr(ins), 1, 1, N, _arr(outs), 0, 1.0, 0, None) == INVALID      # K < 2
+    assert rs(_arr(ins), 65, 1, N, _arr(outs), 0, 1.0, 0, None) == INVALID     # K > 64
+    assert rs(_arr(ins), K, 3, N, _arr(outs), 0, 1.0, 0, None) == INVALID      # M > 2
+    assert rs(_arr(ins), K, 1, N + 1, _arr(outs), 0, 1.0, 0, None) == INVALID  # N % K
+    assert rs(_arr(ins), K, 1, -4, _arr(outs), 0, 1.0, 0, None) == INVALID
+    assert rs(_arr(ins), K, 1, 1 << 36, _arr(outs), 0, 1.0, 0, None) == UNSUP
+    assert rs(_arr(ins), K, 1, N, _arr(outs), 7, 1.0, 0, None) == INVALID      # mode
+    assert rs(None, K, 1, N, _arr(outs), 0, 1.0, 0, None) == INVALID
+    assert rs(_arr(ins[:3] + [0]), K, 1, N, _arr(outs), 0, 1.0, 0, None) == INVALID
+    assert rs(_arr(ins[:3] + [ins[3] + 1]), K, 1, N, _arr(outs), 0, 1.0, 0, None) == ALIGN
+    assert rs(_arr(ins), K, 1, N, _arr(outs[:3] + [outs[3] + 2]), 0, 1.0, 0, None) == ALIGN
+    # outputs overlapping each other / an input
+    assert rs(_arr(ins), K, 1, N, _arr(outs[:3] + [outs[2] + 8]), 0, 1.0, 0, None) == ALIAS
+    assert rs(_arr(ins), K, 1, N, _arr(outs[:3] + [ins[1] + 16]), 0, 1.0, 0, None) == ALIAS
+    # N == 0 is a no-op that touches nothing
+    assert rs(None, K, 1, 0, None, 0, 1.0, 0, None) == OK
+
+
+def test_allgather_rejections(L):
+    K, N = 4, 64
+    S = N // K
+    sh, outs = _bufs(K, 1 << 20), _bufs(K, 1 << 20, BASE + (1 << 30))
+    ag = L.dpr_allgather
+    assert ag(_arr(sh), K, N + 2, _arr(outs), None) == INVALID
+    assert ag(_arr(sh), K, N, _arr(outs[:3] + [outs[3] + 1]), None) == ALIGN
+    assert ag(_arr(sh), K, N, _arr(outs[:3] + [outs[2] + 2 * N - 2]), None) == ALIAS
+    # a shard inside some other rank's output
+    assert ag(_arr(sh[:1] + [outs[0] + 2] + sh[2:]), K, N, _arr(outs), None) == ALIAS
+    # shard j inside out[j] but not at j*S is not the in-place form
+    assert ag(_arr(sh[:2] + [outs[2]] + sh[3:]), K, N, _arr(outs), None) == ALIAS
+
+
+def test_allreduce_rejections(L):
+    K, N = 4, 64
+    ins, outs = _bufs(K, 1 << 20), _bufs(K, 1 << 20, BASE + (1 << 30))
+    ar = L.dpr_allreduce
+    assert ar(_arr(ins), K, N, _arr(outs), 2, 1.0, None) == INVALID
+    # in[1] == out[0]: in-place is only allowed rank by rank
+    assert ar(_arr(ins), K, N, _arr([ins[1]] + outs[1:]), 0, 1.0, None) == ALIAS
+    assert ar(_arr(ins), K, N, _arr(outs[:2] + [outs[1]] + outs[3:]), 0, 1.0, None) == ALIAS
+
+
+def test_flatten_plan_rejections(L):
+    h = ctypes.c_void_p()
+    src = _arr(_bufs(2, 1 << 20))
+    n = (ctypes.c_int64 * 2)(8, 8)
+    o_bad = (ctypes.c_int64 * 2)(0, 4)        # spans overlap
+    assert L.dpr_flatten_plan_create(ctypes.byref(h), 1, 2, src, n, o_bad, 16, None) == ALIAS
+    o_oob = (ctypes.c_int64 * 2)(0, 12)       # second span leaves the bucket
+    assert L.dpr_flatten_plan_create(ctypes.byref(h), 1, 2, src, n, o_oob, 16, None) == INVALID
+    o = (ctypes.c_int64 * 2)(0, 8)
+    odd = _arr([BASE, BASE + (1 << 20) + 1])
+    assert L.dpr_flatten_plan_create(ctypes.byref(h), 1, 2, odd, n, o, 16, None) == ALIGN
+    assert h.value is None
+    assert L.dpr_flatten_plan_destroy(None) == OK
+    assert L.dpr_flatten_bucket(None, None, None) == INVALID
+
+
+def test_strerror_and_version(L):
+    import gradient_reduction_gb300 as g
+    assert g.dpr_strerror(ALIAS) == "buffers overlap"
+    assert "sm_103a" in g.dpr_version()
+    assert L.dpr_last_cuda_error() == 0
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_bucket_assign_matches_oracle(L, seed):
+    import gradient_reduction_gb300 as g
+    rng = random.Random(seed)
+    numel = [rng.choice([1, 3, 8, 100, 4096, 70000]) for _ in range(rng.randint(1, 80))]
+    cap = rng.choice([1, 64, 5000, 100000])
+    pad = rng.choice([1, 2, 8, 64])
+    b_of, off, bn = g.dpr_bucket_assign(numel, cap, pad)
+    ref = ofl.assign_buckets(numel, cap, pad)
+    assert bn == [b.numel for b in ref]
+    for bi, b in enumerate(ref):
+        for p, o in zip(b.params, b.offsets):
+            assert b_of[p] == bi and off[p] == o
+
+
+def test_bucket_assign_config3(L):
+    import gradient_reduction_gb300 as g
+    from workloads import configs as C
+    numel = [n for *_, n in C.CFG3.arrival_order()]
+    _, _, bn = g.dpr_bucket_assign(numel, C.CFG3.bucket_cap, 8)
+    assert bn == [b.numel for b in ofl.assign_buckets(numel, C.CFG3.bucket_cap, 8)]
+    assert len(bn) == 42
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from gradient_reduction_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _binding.lib()

@@ -1,0 +1,80 @@
+"""Host logic of bench.py: the multi-rank harness (barrier, max over ranks,
+whole-job value) under two gloo processes on CPU, and the reference arm's
+JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    r, w, lr = bench.dist_env()
+    bench.barrier()
+    elapsed = 1.0 + rank          # rank 1 is the slow one
+    mx = bench.max_over_ranks(elapsed)
+    val = bench.job_value(1e9, 10, w, mx)
+    bench.barrier()
+    dist.destroy_process_group()
+    q.put((r, w, lr, mx, val))
+
+
+def test_two_rank_harness_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [x[:3] for x in res] == [(0, 2, 0), (1, 2, 1)]
+    for _, _, _, mx, val in res:
+        assert mx == 2.0                     # the slowest rank's time
+        assert val == pytest.approx(1e9 * 10 * 2 / 2.0 / 1e9)
+
+
+def test_job_value_single():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.job_value(2e9, 5, 1, 1.0) == pytest.approx(10.0)
+    assert bench.max_over_ranks(3.5) == 3.5      # no process group: identity
+
+
+def test_reference_arm_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                         cwd=ROOT, timeout=300)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s"
+    assert line["higher_is_better"] is True and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                         cwd=ROOT, env=env, timeout=300)
+    assert out.returncode == 0 and out.stdout.strip() == ""
