@@ -69,6 +69,9 @@ def parse_args(argv=None):
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--only", choices=STEP_KERNELS, default=None,
                    help="profile helper: launch only this kernel per step")
+    p.add_argument("--n-per-rank", type=int, default=None,
+                   help="profile helper: elements per rank (a multiple of 2**24) for a small "
+                        "case; the bench line is quoted only at the default 2**29")
     return p.parse_args(argv)
 
 
@@ -179,13 +182,19 @@ class ClockSampler:
 class Workload:
     """Device-resident buffers of the bench workload and one step's launches."""
 
-    def __init__(self, dev, stream):
+    def __init__(self, dev, stream, n_per_rank=None):
+        import dataclasses
+
         import torch
         import gradient_reduction_gb300 as dpr
         from workloads import configs as C
         from workloads import synthetic as syn
         self.dpr, self.torch = dpr, torch
         w = C.BENCH
+        if n_per_rank is not None and n_per_rank != w.N:
+            if n_per_rank <= 0 or n_per_rank % w.frag_numel:
+                raise ValueError("--n-per-rank must be a positive multiple of 2**24")
+            w = dataclasses.replace(w, N=n_per_rank, n_frag=n_per_rank // w.frag_numel)
         self.w, self.dev, self.stream = w, dev, stream
         K, N = w.K, w.N
         S = N // K
@@ -252,7 +261,7 @@ def run_device(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
-    wl = Workload(dev, stream)
+    wl = Workload(dev, stream, args.n_per_rank)
     kernels = (args.only,) if args.only else STEP_KERNELS
     step_bytes = sum(wl.bytes[k] for k in kernels)
     for _ in range(args.warmup):
@@ -485,6 +494,10 @@ def main(argv=None):
     }
     if args.only:
         line["only"] = args.only
+    if args.n_per_rank:
+        line["config"]["elements_per_rank"] = wl_n = res["wl"].N
+        line["config"]["bytes_per_rank"] = 2 * wl_n
+        line["config"]["workload"] += f"_profile_case_{wl_n}"
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only:
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:

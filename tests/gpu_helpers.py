@@ -72,39 +72,32 @@ def sample_positions(S: int, w: int, seed: int) -> np.ndarray:
     return np.array(sorted(pos), dtype=np.int64)
 
 
-def gather_positions(get_slab, K: int, S: int, T: np.ndarray) -> np.ndarray:
-    """For one rank buffer: its elements at c*S + T for every chunk c, as bf16
-    bits, concatenated chunk by chunk.  get_slab(start, count) -> bf16 tensor."""
-    parts = []
-    # contiguous runs of T keep the number of generator calls small
-    runs = np.split(T, np.flatnonzero(np.diff(T) != 1) + 1)
-    for c in range(K):
-        for run in runs:
-            parts.append(bits(get_slab(c * S + int(run[0]), len(run))))
-    return np.concatenate(parts)
+def chunk_positions(K: int, S: int, T: np.ndarray) -> np.ndarray:
+    """Element indices c*S + T for every chunk c, chunk by chunk."""
+    return np.concatenate([c * S + T for c in range(K)]).astype(np.int64)
 
 
-def gather_inputs(slab_fn, K: int, M: int, S: int, T: np.ndarray) -> list:
+def gather_inputs(at_fn, K: int, M: int, S: int, T: np.ndarray) -> list:
     """Host inputs of the sampled sub-problem: x[m*K + r] = rank r's micro m
-    buffer at c*S + T for every chunk c.  slab_fn(rank, micro, start, count)
-    -> bf16 tensor."""
-    return [gather_positions(lambda s, n, r=r, m=m: slab_fn(r, m, s, n), K, S, T)
-            for m in range(M) for r in range(K)]
+    buffer at c*S + T for every chunk c.  at_fn(rank, micro, idx) -> bf16
+    tensor of the generator's values at those element indices."""
+    idx = chunk_positions(K, S, T)
+    return [bits(at_fn(r, m, idx)) for m in range(M) for r in range(K)]
 
 
-def oracle_rs_sampled(slab_fn, K: int, M: int, S: int, T: np.ndarray, mode: int, scale: float,
+def oracle_rs_sampled(at_fn, K: int, M: int, S: int, T: np.ndarray, mode: int, scale: float,
                       out_init=None, x=None):
     """Oracle reduce-scatter on positions T of every chunk.  Returns K float32
     arrays of |T|."""
     if x is None:
-        x = gather_inputs(slab_fn, K, M, S, T)
+        x = gather_inputs(at_fn, K, M, S, T)
     shards, _ = ring.reduce_scatter(x, K, M, mode, scale, out_init=out_init)
     return shards
 
 
-def oracle_ar_sampled(slab_fn, K: int, S: int, T: np.ndarray, mode: int, scale: float, x=None):
+def oracle_ar_sampled(at_fn, K: int, S: int, T: np.ndarray, mode: int, scale: float, x=None):
     if x is None:
-        x = gather_inputs(slab_fn, K, 1, S, T)
+        x = gather_inputs(at_fn, K, 1, S, T)
     outs, _ = ring.allreduce(x[:K], K, mode, scale)
     return outs           # each: K chunks of |T|, chunk by chunk
 

@@ -33,19 +33,20 @@ def _release():
     torch.cuda.empty_cache()
 
 
-def _check_device_inputs(x, slab_fn, K, M, S, T):
+def _check_device_inputs(x, at_fn, K, M, S, T):
     """Device-generated inputs equal host-generated ones at c*S + T."""
+    idx = H.chunk_positions(K, S, T)
+    didx = torch.from_numpy(idx).to(x[0].device)
     for m in range(M):
         for r in (0, K - 1):
-            dev_bits = np.concatenate([H.bits(H.device_slab_positions(x[m * K + r], c * S, T))
-                                       for c in range(K)])
-            host = H.gather_positions(lambda s, n: slab_fn(r, m, s, n), K, S, T)
+            dev_bits = H.bits(x[m * K + r].index_select(0, didx))
+            host = H.bits(at_fn(r, m, idx))
             assert np.array_equal(dev_bits, host), f"generator mismatch rank {r} micro {m}"
 
 
-def _check_rs_sampled(out, slab_fn, K, M, S, mode, scale, seed, w=64, x=None):
+def _check_rs_sampled(out, at_fn, K, M, S, mode, scale, seed, w=64, x=None):
     T = H.sample_positions(S, w, seed)
-    want = H.oracle_rs_sampled(slab_fn, K, M, S, T, mode, scale, x=x)
+    want = H.oracle_rs_sampled(at_fn, K, M, S, T, mode, scale, x=x)
     idx = torch.from_numpy(T).to(out[0].device)
     for j in range(K):
         got = out[j].index_select(0, idx).cpu().numpy()
@@ -80,28 +81,27 @@ def test_cfg2_reduce_scatter(mode):
     out = [torch.empty(S, dtype=torch.float32, device=dev) for _ in range(K)]
     dpr.dpr_reduce_scatter(x, K, 1, N, out, mode=mode, scale=1.0 / K)
     torch.cuda.synchronize()
-    T = _check_rs_sampled(out, cfg.slab, K, 1, S, mode, 1.0 / K, seed=2 + mode)
-    _check_device_inputs(x, cfg.slab, K, 1, S, T)
+    T = _check_rs_sampled(out, cfg.at, K, 1, S, mode, 1.0 / K, seed=2 + mode)
+    _check_device_inputs(x, cfg.at, K, 1, S, T)
     _rs_error_bound(x, out, K, 1, S, mode)
 
 
 # ---- config 3: fragmented transformer gradients, flatten + reduce-scatter -----------
 
-def _bucket_slab_fn(cfg, bk):
-    """slab(rank, micro, start, count) over a bucket's positions: generator
-    values of the gradient at that offset, zeros in the padding."""
-    starts = bk.offsets
+def _bucket_at_fn(cfg, bk):
+    """at(rank, micro, idx) over a bucket's element indices: the generator's
+    value of the gradient stored there, zero in the padding."""
     numels = [cfg.arrival_order()[p][2] for p in bk.params]
 
-    def slab(rank, _m, start, count):
-        out = torch.zeros(count, dtype=torch.bfloat16)
-        pos, end = start, start + count
-        for p, o, n in zip(bk.params, starts, numels):
-            lo, hi = max(pos, o), min(end, o + n)
-            if lo < hi:
-                out[lo - start:hi - start] = cfg.grad_slab(rank, p, lo - o, hi - lo)
+    def at(rank, _m, idx):
+        idx = np.asarray(idx, dtype=np.int64)
+        out = torch.zeros(len(idx), dtype=torch.bfloat16)
+        for p, o, n in zip(bk.params, bk.offsets, numels):
+            sel = np.flatnonzero((idx >= o) & (idx < o + n))
+            if len(sel):
+                out[torch.from_numpy(sel)] = cfg.grad_at(rank, p, idx[sel] - o)
         return out
-    return slab
+    return at
 
 
 def _run_cfg3(cfg, mode, check_buckets):
@@ -135,7 +135,7 @@ def _run_cfg3(cfg, mode, check_buckets):
         dpr.dpr_reduce_scatter(views, K, 1, b.numel, out, mode=mode, scale=1.0 / K)
         if bi in check_buckets:
             torch.cuda.synchronize()
-            _check_rs_sampled(out, _bucket_slab_fn(cfg, b), K, 1, S, mode, 1.0 / K,
+            _check_rs_sampled(out, _bucket_at_fn(cfg, b), K, 1, S, mode, 1.0 / K,
                               seed=bi, w=32)
         shard_off += S
     torch.cuda.synchronize()
@@ -169,8 +169,7 @@ def test_cfg4_allgather():
         assert torch.equal(out[r].view(torch.int16), full.view(torch.int16)), f"replica {r}"
     del full
     T = H.sample_positions(S, 128, 4)
-    shard_bits = [H.gather_positions(lambda s, n, j=j: C.cfg4_slab(j * S + s, n), 1, S, T)
-                  for j in range(K)]
+    shard_bits = [H.bits(C.cfg4_at(j * S + T)) for j in range(K)]
     want, _ = ring.allgather(shard_bits, K)
     idx = torch.from_numpy(np.concatenate([c * S + T for c in range(K)])).to(dev)
     for r in range(K):
@@ -191,18 +190,18 @@ def _sweep_point(K, nbytes, dev, check_ag_ar):
     x = [cfg.buffer(r, m, device=dev) for m in range(M) for r in range(K)]
     out = [torch.empty(S, dtype=torch.float32, device=dev) for _ in range(K)]
     T = H.sample_positions(S, 16, K + nbytes)
-    xh = H.gather_inputs(cfg.slab, K, M, S, T)
+    xh = H.gather_inputs(cfg.at, K, M, S, T)
     for mode in H.MODES:
         dpr.dpr_reduce_scatter(x, K, M, N, out, mode=mode, scale=1.0 / K)
         torch.cuda.synchronize()
-        _check_rs_sampled(out, cfg.slab, K, M, S, mode, 1.0 / K, seed=K + nbytes, w=16, x=xh)
-    _check_device_inputs(x, cfg.slab, K, M, S, T)
+        _check_rs_sampled(out, cfg.at, K, M, S, mode, 1.0 / K, seed=K + nbytes, w=16, x=xh)
+    _check_device_inputs(x, cfg.at, K, M, S, T)
     if check_ag_ar:
         ar = [torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(K)]
         for mode in H.MODES:
             dpr.dpr_allreduce(x[:K], K, N, ar, mode=mode, scale=1.0 / K)
             torch.cuda.synchronize()
-            want = H.oracle_ar_sampled(cfg.slab, K, S, T, mode, 1.0 / K, x=xh)
+            want = H.oracle_ar_sampled(cfg.at, K, S, T, mode, 1.0 / K, x=xh)
             idx = torch.from_numpy(np.concatenate([c * S + T for c in range(K)])).to(dev)
             for r in (0, K // 2, K - 1):
                 H.assert_bf16_equal(H.bits(ar[r].index_select(0, idx)), want[r], f"AR {r}")

@@ -59,3 +59,12 @@ def test_config_sizes():
     pts = C.cfg5_points()
     assert len(pts) == 55 and (64, 1 << 30) in pts and (2, 1024) in pts
     assert C.BENCH.n_frag * C.BENCH.frag_numel == C.BENCH.N
+
+
+def test_index_evaluation_matches_ranges():
+    idx = np.array([0, 5, 4096, 99_999, 7, 7, 123_456], dtype=np.int64)
+    for cfg in (C.CFG2, C.cfg5(8, 1 << 20)):
+        full = _bits(cfg.slab(1, 0, 0, 123_457))
+        assert np.array_equal(_bits(cfg.at(1, 0, idx)), full[idx])
+    u = _bits(C.cfg4_slab(0, 123_457))
+    assert np.array_equal(_bits(C.cfg4_at(idx)), u[idx])

@@ -45,6 +45,14 @@ class Dist:
             return syn.uniform_bf16(start, count, key, self.scale, device=device, out=out)
         raise ValueError(self.kind)
 
+    def at(self, idx, key: int) -> torch.Tensor:
+        """Host values at arbitrary element indices of the stream `key`."""
+        if self.kind == "gauss":
+            return syn.gauss_bf16_at(idx, key, self.scale, self.outlier_frac, self.outlier_mult)
+        if self.kind == "uniform":
+            return syn.uniform_bf16_at(idx, key, self.scale)
+        raise ValueError(self.kind)
+
 
 @dataclass(frozen=True)
 class Flat:
@@ -66,6 +74,10 @@ class Flat:
     def slab(self, rank: int, micro: int, start: int, count: int, device="cpu", out=None):
         """Elements [start, start+count) of rank `rank`'s micro-batch `micro` buffer."""
         return self.dist.fill(start, count, self.key(rank, micro), device=device, out=out)
+
+    def at(self, rank: int, micro: int, idx) -> torch.Tensor:
+        """Host values of rank `rank`'s micro-batch `micro` buffer at indices idx."""
+        return self.dist.at(idx, self.key(rank, micro))
 
     def buffer(self, rank: int, micro: int = 0, device="cpu", out=None):
         return self.slab(rank, micro, 0, self.N, device=device, out=out)
@@ -141,6 +153,9 @@ class Fragmented:
     def grad_slab(self, rank: int, p: int, start: int, count: int, device="cpu"):
         return self.dist.fill(start, count, self.key(rank, p), device=device)
 
+    def grad_at(self, rank: int, p: int, idx) -> torch.Tensor:
+        return self.dist.at(idx, self.key(rank, p))
+
 
 CFG3 = Fragmented("cfg3_7layer_h4096", 3, K=8, layers=7, dist=Dist("gauss", 1e-3))
 CFG3_224 = Fragmented("cfg3_28layer_h4096_224t", 3, K=8, layers=28, dist=Dist("gauss", 1e-3))
@@ -163,6 +178,10 @@ def cfg4_shard(j: int, device="cpu", out=None):
 
 def cfg4_slab(start: int, count: int, device="cpu"):
     return CFG4.dist.fill(start, count, syn.stream_key(CFG4.seed, 0, 0, 0), device=device)
+
+
+def cfg4_at(idx) -> torch.Tensor:
+    return CFG4.dist.at(idx, syn.stream_key(CFG4.seed, 0, 0, 0))
 
 
 # --- bench workload -------------------------------------------------------------

@@ -84,7 +84,10 @@ def stream_key(seed: int, rank: int, micro: int = 0, tag: int = 0) -> int:
 
 
 def _words(start: int, count: int, key: int, device) -> tuple:
-    idx = torch.arange(start, start + count, dtype=torch.int64, device=device)
+    return _words_at(torch.arange(start, start + count, dtype=torch.int64, device=device), key)
+
+
+def _words_at(idx: torch.Tensor, key: int) -> tuple:
     lo = idx & M32
     hi = idx >> 32
     base = _fmix32(_fmix32(lo ^ key) ^ _mul32(hi, 0x27D4EB2F) ^ fmix32_int(key ^ 0x5BD1E995))
@@ -102,20 +105,44 @@ def gauss_bf16(start: int, count: int, key: int, sigma: float,
     """bf16 values of elements [start, start+count) of the stream `key`."""
     if out is None:
         out = torch.empty(count, dtype=torch.bfloat16, device=device)
-    scale = torch.tensor(float(np.float32(sigma / _IRWIN_HALL4_STD)), dtype=torch.float32,
-                         device=device)
-    mult = torch.tensor(float(np.float32(outlier_mult)), dtype=torch.float32, device=device)
-    thresh = int(outlier_frac * 4294967296.0)
     step = _chunk(device)
     for s in range(0, count, step):
         n = min(step, count - s)
         w0, w1, w2 = _words(start + s, n, key, device)
-        z = (w0 & 0xFFFF) + (w0 >> 16) + (w1 & 0xFFFF) + (w1 >> 16) - _IRWIN_HALL4_MEAN
-        x = z.to(torch.float32) * scale
-        if thresh > 0:
-            x = torch.where(w2 < thresh, x * mult, x)
-        out[s:s + n] = x.to(torch.bfloat16)
+        out[s:s + n] = _gauss_from_words(w0, w1, w2, sigma, outlier_frac, outlier_mult, device)
     return out
+
+
+def _gauss_from_words(w0, w1, w2, sigma, outlier_frac, outlier_mult, device):
+    scale = torch.tensor(float(np.float32(sigma / _IRWIN_HALL4_STD)), dtype=torch.float32,
+                         device=device)
+    z = (w0 & 0xFFFF) + (w0 >> 16) + (w1 & 0xFFFF) + (w1 >> 16) - _IRWIN_HALL4_MEAN
+    x = z.to(torch.float32) * scale
+    thresh = int(outlier_frac * 4294967296.0)
+    if thresh > 0:
+        mult = torch.tensor(float(np.float32(outlier_mult)), dtype=torch.float32, device=device)
+        x = torch.where(w2 < thresh, x * mult, x)
+    return x.to(torch.bfloat16)
+
+
+def gauss_bf16_at(idx, key: int, sigma: float, outlier_frac: float = 0.0,
+                  outlier_mult: float = 100.0) -> torch.Tensor:
+    """gauss_bf16 evaluated at arbitrary element indices (host)."""
+    idx = torch.as_tensor(np.asarray(idx, dtype=np.int64))
+    w0, w1, w2 = _words_at(idx, key)
+    return _gauss_from_words(w0, w1, w2, sigma, outlier_frac, outlier_mult, "cpu")
+
+
+def _uniform_from_word(w0, amp, device):
+    scale = torch.tensor(float(np.float32(amp)) * 2.0 ** -23, dtype=torch.float32, device=device)
+    return (((w0 >> 8) - (1 << 23)).to(torch.float32) * scale).to(torch.bfloat16)
+
+
+def uniform_bf16_at(idx, key: int, amp: float) -> torch.Tensor:
+    """uniform_bf16 evaluated at arbitrary element indices (host)."""
+    idx = torch.as_tensor(np.asarray(idx, dtype=np.int64))
+    w0, _, _ = _words_at(idx, key)
+    return _uniform_from_word(w0, amp, "cpu")
 
 
 def uniform_bf16(start: int, count: int, key: int, amp: float, device="cpu",
@@ -123,13 +150,11 @@ def uniform_bf16(start: int, count: int, key: int, amp: float, device="cpu",
     """bf16 values on [-amp, amp) of elements [start, start+count) of stream `key`."""
     if out is None:
         out = torch.empty(count, dtype=torch.bfloat16, device=device)
-    scale = torch.tensor(float(np.float32(amp)) * 2.0 ** -23, dtype=torch.float32, device=device)
     step = _chunk(device)
     for s in range(0, count, step):
         n = min(step, count - s)
         w0, _, _ = _words(start + s, n, key, device)
-        z = (w0 >> 8) - (1 << 23)
-        out[s:s + n] = (z.to(torch.float32) * scale).to(torch.bfloat16)
+        out[s:s + n] = _uniform_from_word(w0, amp, device)
     return out
 
 
