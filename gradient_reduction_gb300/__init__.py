@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     dpr_allreduce,
     dpr_bucket_assign,
     dpr_flatten_bucket,
+    dpr_flatten_bucket_noalloc,
     dpr_flatten_plan_create,
     dpr_flatten_plan_destroy,
     dpr_reduce_scatter,

@@ -36,6 +36,8 @@ _SIGS = {
     "dpr_bucket_assign": [_i64p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                           ctypes.POINTER(ctypes.c_int32), _i64p, _i64p,
                           ctypes.POINTER(ctypes.c_int)],
+    "dpr_flatten_bucket_noalloc": [ctypes.c_int, ctypes.c_int, _pp, _i64p, _i64p, ctypes.c_int64,
+                                   _pp, _c_p],
     "dpr_strerror": [ctypes.c_int],
     "dpr_last_cuda_error": [],
     "dpr_version": [],
@@ -193,6 +195,32 @@ def dpr_flatten_bucket(plan: FlattenPlan, dst: Sequence[torch.Tensor], stream=No
 
 def dpr_flatten_plan_destroy(plan: FlattenPlan) -> None:
     plan.close()
+
+
+def dpr_flatten_bucket_noalloc(srcs: Sequence[Sequence[torch.Tensor]], numel: Sequence[int],
+                               offset: Sequence[int], bucket_numel: int,
+                               dst: Sequence[torch.Tensor], stream=None) -> None:
+    """The flat-bucket gather without any device allocation, for callers that
+    cannot call cudaMalloc (see include/dpr.h).  Same arguments as
+    dpr_flatten_plan_create plus the destinations of dpr_flatten_bucket."""
+    K, P = len(srcs), len(numel)
+    flat = []
+    for r in range(K):
+        if len(srcs[r]) != P:
+            raise ValueError("every rank needs P gradients")
+        for p in range(P):
+            t = srcs[r][p]
+            if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError("gradients must be contiguous CUDA bf16 tensors")
+            if t.numel() != numel[p]:
+                raise ValueError(f"gradient {p} of rank {r}: {t.numel()} elements, numel says {numel[p]}")
+            flat.append(t)
+    _need(dst, K, torch.bfloat16, bucket_numel, "dst")
+    n_arr = (ctypes.c_int64 * max(P, 1))(*numel)
+    o_arr = (ctypes.c_int64 * max(P, 1))(*offset)
+    st = lib().dpr_flatten_bucket_noalloc(K, P, _ptrs(flat), n_arr, o_arr, bucket_numel,
+                                          _ptrs(dst), _stream(stream))
+    _check("dpr_flatten_bucket_noalloc", st)
 
 
 def dpr_bucket_assign(numel: Sequence[int], cap: int, pad_to: int = 1):

@@ -155,6 +155,41 @@ dpr_status dpr_flatten_bucket(const dpr_flatten_plan* plan, void* const* dst, vo
 dpr_status dpr_flatten_plan_destroy(dpr_flatten_plan* plan);
 
 /*
+ * Flat-bucket gather that allocates nothing.  The pages have no counterpart
+ * of this call; it exists for callers that cannot call cudaMalloc: a process
+ * whose device memory a caching allocator has already reserved (a separate
+ * cudaMalloc fails or fragments its pool), a plug-in whose host forbids
+ * allocation after start-up, or a loop that cannot afford cudaMalloc and
+ * cudaFree, which may synchronise the whole device.
+ *
+ * Same copy as dpr_flatten_plan_create + dpr_flatten_bucket, with the same
+ * argument meanings and checks, in one call: the segment table is built on
+ * the host and copied (cudaMemcpyAsync on `stream`) into a fixed array
+ * compiled into the library, then one kernel does the gather.  Limits and
+ * sharing:
+ *   - at most DPR_NOALLOC_MAX_SEGMENTS (rank, non-empty gradient) pairs per
+ *     call, i.e. K * P_nonempty <= 4096; larger calls return
+ *     DPR_ERR_UNSUPPORTED and do nothing.  The array (160 KiB) is held by
+ *     every GPU that loads the library until the process exits;
+ *   - every call shares that array and overwrites the entries it uses (no
+ *     entry needs to start at zero).  Calls ordered on one stream are safe;
+ *     calls that overlap on the GPU (different streams, or other host threads'
+ *     streams, without ordering between them) race on the table and must be
+ *     avoided;
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture;
+ *   - the host table is copied from pageable memory, so the call returns
+ *     only after the copy has been staged;
+ *   - on DPR_ERR_CUDA the CUDA error is left for cudaGetLastError().
+ */
+#define DPR_NOALLOC_MAX_SEGMENTS 4096
+
+dpr_status dpr_flatten_bucket_noalloc(int K, int P, const void* const* src, const int64_t* numel,
+                                      const int64_t* offset, int64_t bucket_numel,
+                                      void* const* dst, void* stream);
+
+/*
  * Bucket formation, host only (DeepSpeed ZeRO-3 source walkthrough, sections
  * 3.1, 5.1, 5.4): gradients in arrival order are appended at the running
  * offset; the bucket is flushed first when adding the next gradient would

@@ -35,7 +35,7 @@ def _declared():
 
 def test_exports_every_declared_function(L):
     names = _declared()
-    assert len(names) == 10
+    assert len(names) == 11
     for n in names:
         assert hasattr(L, n), n
 
