@@ -62,7 +62,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["dpr", "reference"], default="dpr")
-    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--e2e-steps", type=int, default=8)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -180,9 +180,15 @@ class ClockSampler:
 # ---- the device workload -----------------------------------------------------------
 
 class Workload:
-    """Device-resident buffers of the bench workload and one step's launches."""
+    """Device-resident buffers of the bench workload and one step's launches.
 
-    def __init__(self, dev, stream, n_per_rank=None):
+    Each kind of buffer is one contiguous allocation with one row per rank
+    (fragments: one row per rank and fragment), so that host<->device copies
+    move each kind in one call.  With fill=False the buffers are left
+    uninitialised (a second buffer set for the pipelined end-to-end steps,
+    whose inputs arrive from the host)."""
+
+    def __init__(self, dev, stream, n_per_rank=None, fill=True):
         import dataclasses
 
         import torch
@@ -202,17 +208,32 @@ class Workload:
         self.K, self.N, self.S, self.F, self.P = K, N, S, F, P
         bf, f32 = torch.bfloat16, torch.float32
         with torch.cuda.stream(stream):
-            self.frags = [[w.dist.fill(0, F, w.frag_key(r, p), device=dev).view(*w.frag_shape)
-                           for p in range(P)] for r in range(K)]
-            self.ipg0 = [w.dist.fill(0, N, w.micro0_key(r), device=dev) for r in range(K)]
-            self.ipg1 = [torch.zeros(N, dtype=bf, device=dev) for _ in range(K)]
-            self.part_f32 = [torch.empty(S, dtype=f32, device=dev) for _ in range(K)]
-            self.part_hop = [syn.gauss_bf16(0, S, w.prev_grad_key(j), 1e-3, device=dev).float()
-                             for j in range(K)]
-            self.shards = [w.param_dist.fill(j * S, S, w.param_key(), device=dev)
-                           for j in range(K)]
-            self.params = [torch.empty(N, dtype=bf, device=dev) for _ in range(K)]
-            self.ar_out = [torch.empty(N, dtype=bf, device=dev) for _ in range(K)]
+            self.frag_all = torch.empty(K * P, F, dtype=bf, device=dev)
+            self.ipg0_all = torch.empty(K, N, dtype=bf, device=dev)
+            self.ipg1_all = torch.zeros(K, N, dtype=bf, device=dev)
+            self.part_f32_all = torch.empty(K, S, dtype=f32, device=dev)
+            self.part_hop_all = torch.empty(K, S, dtype=f32, device=dev)
+            self.shards_all = torch.empty(K, S, dtype=bf, device=dev)
+            self.params_all = torch.empty(K, N, dtype=bf, device=dev)
+            self.ar_all = torch.empty(K, N, dtype=bf, device=dev)
+            if fill:
+                for r in range(K):
+                    for p in range(P):
+                        w.dist.fill(0, F, w.frag_key(r, p), device=dev,
+                                    out=self.frag_all[r * P + p])
+                    w.dist.fill(0, N, w.micro0_key(r), device=dev, out=self.ipg0_all[r])
+                    self.part_hop_all[r].copy_(
+                        syn.gauss_bf16(0, S, w.prev_grad_key(r), 1e-3, device=dev))
+                    w.param_dist.fill(r * S, S, w.param_key(), device=dev, out=self.shards_all[r])
+            self.frags = [[self.frag_all[r * P + p].view(*w.frag_shape) for p in range(P)]
+                          for r in range(K)]
+            self.ipg0 = list(self.ipg0_all.unbind(0))
+            self.ipg1 = list(self.ipg1_all.unbind(0))
+            self.part_f32 = list(self.part_f32_all.unbind(0))
+            self.part_hop = list(self.part_hop_all.unbind(0))
+            self.shards = list(self.shards_all.unbind(0))
+            self.params = list(self.params_all.unbind(0))
+            self.ar_out = list(self.ar_all.unbind(0))
             self.plan = dpr.dpr_flatten_plan_create(
                 self.frags, [F] * P, [p * F for p in range(P)], N, stream=stream)
         stream.synchronize()
@@ -224,6 +245,13 @@ class Workload:
             "allreduce": 4 * K * N,
         }
         self.launches_per_step = len(STEP_KERNELS)
+
+    # inputs a step reads from the host, outputs it returns (e2e steps)
+    def inputs(self):
+        return [self.frag_all, self.ipg0_all, self.part_hop_all, self.shards_all]
+
+    def outputs(self):
+        return [self.part_f32_all, self.part_hop_all, self.params_all, self.ar_all]
 
     def launch(self, name):
         dpr, K, N, s = self.dpr, self.K, self.N, self.stream
@@ -301,62 +329,81 @@ def run_device(args, rank, world, local_rank):
 
 
 def run_e2e(wl, args, step_bytes):
-    """Steps through the public API from host memory: the step's inputs are
-    copied from pinned host buffers, the five launches run, and every result
-    is read back into pinned host buffers, all inside the timed region."""
+    """End-to-end steps through the public API from host memory.
+
+    Every timed step copies its inputs (gradient fragments, the other micro-
+    batch's bucket, the fp32 partition it accumulates into, the parameter
+    shards) from pinned host buffers, runs the five launches, and reads every
+    result (both fp32 partitions, the all-gathered parameters, the all-reduced
+    bucket) back into pinned host buffers.  Copies in, kernels and copies out
+    run on three streams over two device buffer sets, so step i+1's inputs
+    and step i-1's results cross the host link while step i computes; each
+    step still moves all of its own bytes inside the timed region."""
     import torch
-    s = wl.stream
-    pin = dict(pin_memory=True)
-    K, P, F, N, S = wl.K, wl.P, wl.F, wl.N, wl.S
-    h_frags = torch.empty(K * P, F, dtype=torch.bfloat16, **pin)
-    h_ipg0 = torch.empty(K, N, dtype=torch.bfloat16, **pin)
-    h_part = torch.empty(K, S, dtype=torch.float32, **pin)
-    h_shards = torch.empty(K, S, dtype=torch.bfloat16, **pin)
-    o_f32 = torch.empty(K, S, dtype=torch.float32, **pin)
-    o_hop = torch.empty(K, S, dtype=torch.float32, **pin)
-    o_params = torch.empty(K, N, dtype=torch.bfloat16, **pin)
-    o_ar = torch.empty(K, N, dtype=torch.bfloat16, **pin)
-    with torch.cuda.stream(s):
-        for r in range(K):
-            for p in range(P):
-                h_frags[r * P + p].copy_(wl.frags[r][p].view(-1))
-            h_ipg0[r].copy_(wl.ipg0[r])
-            h_part[r].copy_(wl.part_hop[r])
-            h_shards[r].copy_(wl.shards[r])
-    s.synchronize()
-    h2d = (h_frags.numel() + h_ipg0.numel() + h_shards.numel()) * 2 + h_part.numel() * 4
-    d2h = (o_f32.numel() + o_hop.numel()) * 4 + (o_params.numel() + o_ar.numel()) * 2
+    dev = wl.dev
+    sets = [wl, Workload(dev, wl.stream, args.n_per_rank, fill=False)]
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl.inputs()]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl.outputs()]
+    for h, d in zip(h_in, wl.inputs()):
+        h.copy_(d)
+    torch.cuda.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    s_in, s_out, s_comp = (torch.cuda.Stream(device=dev) for _ in range(3))
+    for w in sets:
+        w.stream = s_comp
+    n = args.e2e_steps
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [None, None]
+    out_done = [None, None]
 
-    def one_step():
-        with torch.cuda.stream(s):
-            for r in range(K):
-                for p in range(P):
-                    wl.frags[r][p].view(-1).copy_(h_frags[r * P + p], non_blocking=True)
-                wl.ipg0[r].copy_(h_ipg0[r], non_blocking=True)
-                wl.part_hop[r].copy_(h_part[r], non_blocking=True)
-                wl.shards[r].copy_(h_shards[r], non_blocking=True)
-            wl.step(STEP_KERNELS)
-            for r in range(K):
-                o_f32[r].copy_(wl.part_f32[r], non_blocking=True)
-                o_hop[r].copy_(wl.part_hop[r], non_blocking=True)
-                o_params[r].copy_(wl.params[r], non_blocking=True)
-                o_ar[r].copy_(wl.ar_out[r], non_blocking=True)
+    def run(steps):
+        for i in range(steps):
+            b = i % 2
+            w = sets[b]
+            # copies in: wait until step i-2 has finished with this set
+            if comp_done[b] is not None:
+                s_in.wait_event(comp_done[b])
+            if out_done[b] is not None:
+                s_in.wait_event(out_done[b])
+            with torch.cuda.stream(s_in):
+                for d, h in zip(w.inputs(), h_in):
+                    d.copy_(h, non_blocking=True)
+            in_done[b].record(s_in)
+            s_comp.wait_event(in_done[b])
+            w.step(STEP_KERNELS)
+            ev = torch.cuda.Event()
+            ev.record(s_comp)
+            comp_done[b] = ev
+            s_out.wait_event(ev)
+            with torch.cuda.stream(s_out):
+                for h, d in zip(h_out, w.outputs()):
+                    h.copy_(d, non_blocking=True)
+            ev2 = torch.cuda.Event()
+            ev2.record(s_out)
+            out_done[b] = ev2
 
-    one_step()
-    s.synchronize()
+    run(2)                                   # warm-up of both buffer sets
+    torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(s)
-    for _ in range(args.e2e_steps):
-        one_step()
-    t1.record(s)
-    s.synchronize()
+    t0.record(s_in)
+    s_comp.wait_event(t0)
+    s_out.wait_event(t0)
+    run(n)
+    s_in.wait_event(out_done[(n - 1) % 2])
+    t1.record(s_in)
+    torch.cuda.synchronize()
     el = t0.elapsed_time(t1) / 1e3
-    el = max_over_ranks(el, wl.dev)
+    el = max_over_ranks(el, dev)
     _, world, _ = dist_env()
-    return {"value": round(job_value(step_bytes, args.e2e_steps, world, el), 1), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "ms_per_step": round(el / args.e2e_steps * 1e3, 3)}
+    sets[1].plan.close()
+    for w in sets:
+        w.stream = wl.stream
+    return {"value": round(job_value(step_bytes, n, world, el), 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": round(el / n * 1e3, 3),
+            "pipelining": "copies in / kernels / copies out on three streams, two buffer sets"}
 
 
 # ---- CPU oracle baseline ---------------------------------------------------------
