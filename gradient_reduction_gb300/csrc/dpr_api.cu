@@ -122,19 +122,22 @@ dpr_status dpr_reduce_scatter(const void* const* in, int K, int M, int64_t N, fl
     if (N == 0) return DPR_OK;
     if (!in || !out) return DPR_ERR_INVALID_ARG;
     const int64_t S = N / K;
-    bool vec = (S % 8) == 0;
+    bool a16 = true, a32 = true;
     std::vector<Span> outs;
     for (int i = 0; i < M * K; ++i) {
         if (!in[i]) return DPR_ERR_INVALID_ARG;
         if (!aligned(in[i], 2)) return DPR_ERR_ALIGNMENT;
-        vec = vec && aligned(in[i], 16);
+        a16 = a16 && aligned(in[i], 16);
+        a32 = a32 && aligned(in[i], 32);
     }
     for (int j = 0; j < K; ++j) {
         if (!out[j]) return DPR_ERR_INVALID_ARG;
         if (!aligned(out[j], 4)) return DPR_ERR_ALIGNMENT;
-        vec = vec && aligned(out[j], 16);
+        a16 = a16 && aligned(out[j], 16);
+        a32 = a32 && aligned(out[j], 32);
         outs.push_back(span_of(out[j], uint64_t(S) * 4));
     }
+    const int width = access_width(S, a32, a16);
     if (!pairwise_disjoint(outs)) return DPR_ERR_ALIAS;
     for (int i = 0; i < M * K; ++i) {
         const Span a = span_of(in[i], uint64_t(N) * 2);
@@ -146,12 +149,12 @@ dpr_status dpr_reduce_scatter(const void* const* in, int K, int M, int64_t N, fl
     for (int i = 0; i < M * K; ++i) p.in[i] = static_cast<const uint16_t*>(in[i]);
     for (int j = 0; j < K; ++j) p.out[j] = out[j];
     p.S = S;
-    p.su = uint32_t(S / 8);
+    p.su = width > 0 ? uint32_t(S / (2 * width)) : 0;
     p.K = K;
     p.M = M;
     p.scale = scale;
     p.accumulate = accumulate ? 1 : 0;
-    return cuda_status(launch_reduce_scatter(p, mode, vec, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_reduce_scatter(p, mode, width, static_cast<cudaStream_t>(stream)));
 }
 
 dpr_status dpr_allgather(const void* const* shard, int K, int64_t N, void* const* out,
@@ -161,18 +164,21 @@ dpr_status dpr_allgather(const void* const* shard, int K, int64_t N, void* const
     if (N == 0) return DPR_OK;
     if (!shard || !out) return DPR_ERR_INVALID_ARG;
     const int64_t S = N / K;
-    bool vec = (S % 8) == 0;
+    bool a16 = true, a32 = true;
     std::vector<Span> outs;
     for (int r = 0; r < K; ++r) {
         if (!shard[r] || !out[r]) return DPR_ERR_INVALID_ARG;
         if (!aligned(shard[r], 2) || !aligned(out[r], 2)) return DPR_ERR_ALIGNMENT;
-        vec = vec && aligned(shard[r], 16) && aligned(out[r], 16);
+        a16 = a16 && aligned(shard[r], 16) && aligned(out[r], 16);
+        a32 = a32 && aligned(shard[r], 32) && aligned(out[r], 32);
         outs.push_back(span_of(out[r], uint64_t(N) * 2));
     }
     if (!pairwise_disjoint(outs)) return DPR_ERR_ALIAS;
+    uint64_t in_place_mask = 0;
     for (int j = 0; j < K; ++j) {
         const bool in_place = shard[j] == static_cast<const void*>(
                                              static_cast<const uint16_t*>(out[j]) + j * S);
+        if (in_place) in_place_mask |= uint64_t(1) << j;
         const Span a = span_of(shard[j], uint64_t(S) * 2);
         for (int r = 0; r < K; ++r) {
             if (in_place && r == j) continue;
@@ -186,9 +192,11 @@ dpr_status dpr_allgather(const void* const* shard, int K, int64_t N, void* const
         p.out[r] = static_cast<uint16_t*>(out[r]);
     }
     p.S = S;
-    p.su = uint32_t(S / 8);
+    p.tiles_per_chunk = uint64_t((S + kAgTile - 1) / kAgTile);
+    p.in_place = in_place_mask;
     p.K = K;
-    return cuda_status(launch_allgather(p, vec, static_cast<cudaStream_t>(stream)));
+    const int width = access_width(S, a32, a16);
+    return cuda_status(launch_allgather(p, width, static_cast<cudaStream_t>(stream)));
 }
 
 dpr_status dpr_allreduce(const void* const* in, int K, int64_t N, void* const* out, int mode,
@@ -199,14 +207,16 @@ dpr_status dpr_allreduce(const void* const* in, int K, int64_t N, void* const* o
     if (N == 0) return DPR_OK;
     if (!in || !out) return DPR_ERR_INVALID_ARG;
     const int64_t S = N / K;
-    bool vec = (S % 8) == 0;
+    bool a16 = true, a32 = true;
     std::vector<Span> outs;
     for (int r = 0; r < K; ++r) {
         if (!in[r] || !out[r]) return DPR_ERR_INVALID_ARG;
         if (!aligned(in[r], 2) || !aligned(out[r], 2)) return DPR_ERR_ALIGNMENT;
-        vec = vec && aligned(in[r], 16) && aligned(out[r], 16);
+        a16 = a16 && aligned(in[r], 16) && aligned(out[r], 16);
+        a32 = a32 && aligned(in[r], 32) && aligned(out[r], 32);
         outs.push_back(span_of(out[r], uint64_t(N) * 2));
     }
+    const int width = access_width(S, a32, a16);
     if (!pairwise_disjoint(outs)) return DPR_ERR_ALIAS;
     for (int i = 0; i < K; ++i) {
         const Span a = span_of(in[i], uint64_t(N) * 2);
@@ -222,10 +232,10 @@ dpr_status dpr_allreduce(const void* const* in, int K, int64_t N, void* const* o
         p.out[r] = static_cast<uint16_t*>(out[r]);
     }
     p.S = S;
-    p.su = uint32_t(S / 8);
+    p.su = width > 0 ? uint32_t(S / (2 * width)) : 0;
     p.K = K;
     p.scale = scale;
-    return cuda_status(launch_allreduce(p, mode, vec, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_allreduce(p, mode, width, static_cast<cudaStream_t>(stream)));
 }
 
 dpr_status dpr_flatten_plan_create(dpr_flatten_plan** plan, int K, int P, const void* const* src,

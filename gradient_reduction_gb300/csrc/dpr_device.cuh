@@ -43,6 +43,53 @@ __device__ __forceinline__ void st_f4(float* p, float a, float b, float c, float
                  : "memory");
 }
 
+// 32-byte accesses (sm_100 and later): the fastest way to stream HBM on GB300.
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                   "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void ld_v8(const void* p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                   "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void st_v8(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_f8(float* p, const float* f) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(f[0]),
+                 "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7])
+                 : "memory");
+}
+
+// W 32-bit words (2W bf16 elements) per rank and access: W = 8 moves 32 bytes
+// (buffers 32-byte aligned), W = 4 moves 16 bytes (16-byte aligned).
+template <int W, bool NC>
+__device__ __forceinline__ void load_words(const uint16_t* p, uint32_t (&w)[W]) {
+    static_assert(W == 4 || W == 8, "16- or 32-byte accesses");
+    if constexpr (W == 8) {
+        if constexpr (NC) ld_nc_v8(p, w);
+        else ld_v8(p, w);
+    } else {
+        const uint4 v = NC ? ld_nc_v4(p) : ld_v4(p);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void store_words(uint16_t* p, const uint32_t (&w)[W]) {
+    if constexpr (W == 8) st_v8(p, w);
+    else st_v4(p, make_uint4(w[0], w[1], w[2], w[3]));
+}
+
 // bf16 -> fp32 is exact: the bf16 bits are the upper half of the fp32 bits.
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -18,7 +18,7 @@ struct RsParams {
     const uint16_t* in[DPR_MAX_MICRO * DPR_MAX_RANKS];  // in[m*K + r]
     float* out[DPR_MAX_RANKS];                          // partition shard j
     int64_t S;          // elements per chunk
-    uint32_t su;        // 8-element units per chunk (vector kernels)
+    uint32_t su;        // 2*width-element units per chunk (vector kernels)
     int K;
     int M;
     float scale;
@@ -38,7 +38,8 @@ struct AgParams {
     const uint16_t* shard[DPR_MAX_RANKS];
     uint16_t* out[DPR_MAX_RANKS];
     int64_t S;
-    uint32_t su;
+    uint64_t tiles_per_chunk;   // ceil(S / kAgTile) (vector kernel)
+    uint64_t in_place;          // bit j: shard[j] == out[j] + j*S
     int K;
 };
 
@@ -59,13 +60,24 @@ struct FlatParams {
     uint16_t* dst[DPR_MAX_RANKS];
 };
 
-constexpr int64_t kFlatTile = 8192;     // elements per flatten tile (16 KB)
+constexpr int64_t kFlatTile = 4096;     // elements per flatten tile (8 KB), one block each
+constexpr int kAgTile = 8192;           // elements per all-gather tile (16 KB), one block each
 
-// Launchers: return cudaSuccess or the launch error.  `vec` selects the
-// 16-byte kernels (all buffers 16-byte aligned and S % 8 == 0).
-cudaError_t launch_reduce_scatter(const RsParams& p, int mode, bool vec, cudaStream_t s);
-cudaError_t launch_allreduce(const ArParams& p, int mode, bool vec, cudaStream_t s);
-cudaError_t launch_allgather(const AgParams& p, bool vec, cudaStream_t s);
+// Access width of the vector kernels, in 32-bit words per rank and access:
+// 8 (32-byte accesses) when every buffer is 32-byte aligned and S % 16 == 0,
+// 4 (16-byte) when every buffer is 16-byte aligned and S % 8 == 0, else 0
+// (element-wise kernels).
+inline int access_width(int64_t S, bool aligned32, bool aligned16) {
+    if (aligned32 && S % 16 == 0) return 8;
+    if (aligned16 && S % 8 == 0) return 4;
+    return 0;
+}
+
+// Launchers: return cudaSuccess or the launch error.  `width` as above;
+// RsParams::su / ArParams::su hold S / (2 * width) when width > 0.
+cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaStream_t s);
+cudaError_t launch_allreduce(const ArParams& p, int mode, int width, cudaStream_t s);
+cudaError_t launch_allgather(const AgParams& p, int width, cudaStream_t s);
 cudaError_t launch_flatten(const FlatParams& p, cudaStream_t s);
 
 // Grid helper: blocks per chunk so that K chunks together fill the GPU with
