@@ -53,7 +53,15 @@ STEP_KERNELS = ("flatten", "rs_fp32_m2", "rs_hop_m2_acc", "allgather", "allreduc
 # DRAM traffic per launch from one ncu capture of each kernel (read + write
 # bytes, scaled to the bench's launch size), valid only while the kernel
 # sources hash to `src_sha`; otherwise reported as null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum at the bench's full size
+    # (K=8, N=2**29), one launch each (profiles/step_k8_1GiB_dram_traffic.md)
+    "flatten": {"bytes": 17_128_000_000, "src_sha": "f9e4c54467eb0af7"},
+    "rs_fp32_m2": {"bytes": 19_312_000_000, "src_sha": "f9e4c54467eb0af7"},
+    "rs_hop_m2_acc": {"bytes": 21_461_000_000, "src_sha": "f9e4c54467eb0af7"},
+    "allgather": {"bytes": 9_601_000_000, "src_sha": "f9e4c54467eb0af7"},
+    "allreduce": {"bytes": 17_121_000_000, "src_sha": "f9e4c54467eb0af7"},
+}
 
 
 def parse_args(argv=None):

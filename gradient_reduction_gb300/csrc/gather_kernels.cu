@@ -32,6 +32,16 @@ __global__ void __launch_bounds__(kThreads) ag_vec(const __grid_constant__ AgPar
     const uint16_t* src = p.shard[j] + t0;
     uint16_t* dst = p.out[r] + j * S + t0;
     constexpr int E = 2 * W;
+    if (n == uint64_t(kAgTile)) {             // full tile: no per-unit guard
+#pragma unroll
+        for (int u = 0; u < kAgTile / E / kThreads; ++u) {
+            const int i = (u * kThreads + int(threadIdx.x)) * E;
+            uint32_t w[W];
+            load_words<W, true>(src + i, w);
+            store_words<W>(dst + i, w);
+        }
+        return;
+    }
 #pragma unroll
     for (int u = 0; u < kAgTile / E / kThreads; ++u) {
         const uint64_t i = uint64_t(u * kThreads + threadIdx.x) * E;
@@ -109,7 +119,20 @@ __global__ void __launch_bounds__(kThreads) flatten_kernel(const __grid_constant
     const int64_t t0 = (tile - sg.tile0) * kFlatTile;
     const int64_t rem = sg.numel - t0;
     const int64_t n = rem < kFlatTile ? rem : kFlatTile;
-    copy_tile(sg.src + t0, p.dst[sg.rank] + sg.dst_off + t0, n);
+    const uint16_t* src = sg.src + t0;
+    uint16_t* dst = p.dst[sg.rank] + sg.dst_off + t0;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
+    if (n == kFlatTile && (a & 31u) == 0) {  // full, 32-byte aligned tile: fixed trip count
+#pragma unroll
+        for (int u = 0; u < int(kFlatTile) / 16 / kThreads; ++u) {
+            const int i = (u * kThreads + int(threadIdx.x)) * 16;
+            uint32_t w[8];
+            load_words<8, true>(src + i, w);
+            store_words<8>(dst + i, w);
+        }
+        return;
+    }
+    copy_tile(src, dst, n);
 }
 
 }  // namespace
