@@ -49,6 +49,7 @@ METRIC = "reduce-scatter/all-gather effective HBM GB/s at K=8, 1 GB/rank; % of G
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 STEP_KERNELS = ("flatten", "rs_fp32_m2", "rs_hop_m2_acc", "allgather", "allreduce")
+Z3_KERNELS = ("rs_coalesced", "ag_coalesced")
 
 # DRAM traffic per launch from one ncu capture of each kernel (read + write
 # bytes, scaled to the bench's launch size), valid only while the kernel
@@ -75,7 +76,10 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
-    p.add_argument("--only", choices=STEP_KERNELS, default=None,
+    p.add_argument("--workload", choices=["zero_bucket", "zero3_per_param"], default="zero_bucket",
+                   help="zero_bucket: the headline step (default); zero3_per_param: the ZeRO-3 "
+                        "discrete path on config 3's 56 gradients")
+    p.add_argument("--only", choices=STEP_KERNELS + Z3_KERNELS, default=None,
                    help="profile helper: launch only this kernel per step")
     p.add_argument("--n-per-rank", type=int, default=None,
                    help="profile helper: elements per rank (a multiple of 2**24) for a small "
@@ -292,13 +296,67 @@ class Workload:
                 self.launch(name)
 
 
+class Zero3Workload:
+    """The ZeRO-3 discrete path on config 3: K=8 ranks, 56 separately allocated
+    gradients of a 7-layer hidden-4096 transformer per rank.  A step
+    reduce-scatters every gradient into per-parameter shards (fp32 partitions,
+    ring fp32, x1/8) and all-gathers bf16 partitions back into 56 full
+    parameters per rank."""
+    kernels = Z3_KERNELS
+
+    def __init__(self, dev, stream):
+        import torch
+        import gradient_reduction_gb300 as dpr
+        from workloads import configs as C
+        self.dpr, self.torch, self.dev, self.stream = dpr, torch, dev, stream
+        cfg = C.CFG3
+        K = cfg.K
+        arr = cfg.arrival_order()
+        numel = [n for *_, n in arr]
+        with torch.cuda.stream(stream):
+            self.grads = [[cfg.grad(r, p, device=dev) for p in range(len(arr))] for r in range(K)]
+            self.params = [[torch.empty(n, dtype=torch.bfloat16, device=dev) for n in numel]
+                           for _ in range(K)]
+            self.rs_plan = dpr.dpr_coalesced_plan_create(self.grads, numel, stream=stream)
+            self.ag_plan = dpr.dpr_coalesced_plan_create(self.params, numel, stream=stream)
+            L = self.rs_plan.partition_numel
+            self.part = [torch.empty(L, dtype=torch.float32, device=dev) for _ in range(K)]
+            self.shards = [torch.empty(L, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+            for j in range(K):
+                self.shards[j].copy_(cfg.dist.fill(0, L, cfg.key(j, 10_000), device=dev))
+        stream.synchronize()
+        N = sum(numel)
+        self.K, self.N, self.L = K, N, L
+        self.bytes = {"rs_coalesced": 2 * K * N + 4 * K * L, "ag_coalesced": 2 * K * L + 2 * K * N}
+
+    def launch(self, name):
+        dpr, s = self.dpr, self.stream
+        if name == "rs_coalesced":
+            dpr.dpr_reduce_scatter_coalesced(self.rs_plan, self.part, mode=dpr.RING_FP32,
+                                             scale=1.0 / self.K, stream=s)
+        elif name == "ag_coalesced":
+            dpr.dpr_allgather_coalesced(self.ag_plan, self.shards, stream=s)
+        else:
+            raise ValueError(name)
+
+    step = Workload.step
+
+    def close(self):
+        self.rs_plan.close()
+        self.ag_plan.close()
+
+
 def run_device(args, rank, world, local_rank):
     import torch
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
-    wl = Workload(dev, stream, args.n_per_rank)
-    kernels = (args.only,) if args.only else STEP_KERNELS
+    if args.workload == "zero3_per_param":
+        wl = Zero3Workload(dev, stream)
+        kernels = (args.only,) if args.only else Z3_KERNELS
+    else:
+        wl = Workload(dev, stream, args.n_per_rank)
+        kernels = (args.only,) if args.only else STEP_KERNELS
     step_bytes = sum(wl.bytes[k] for k in kernels)
     for _ in range(args.warmup):
         wl.step(kernels)
@@ -329,7 +387,7 @@ def run_device(args, rank, world, local_rank):
                              "gbs": wl.bytes[name] / avg / 1e9, "launches": len(ts),
                              "time_share": sum(ts) / sum(sum(v) for v in per.values())}
     e2e = None
-    if not args.no_e2e and not args.only:
+    if not args.no_e2e and not args.only and args.workload == "zero_bucket":
         e2e = run_e2e(wl, args, step_bytes)
     return {"elapsed": elapsed, "max_elapsed": max_elapsed, "step_bytes": step_bytes,
             "kernels": kernels_out, "clocks": clk, "e2e": e2e, "wl": wl,
@@ -553,11 +611,22 @@ def main(argv=None):
         line["config"]["elements_per_rank"] = wl_n = res["wl"].N
         line["config"]["bytes_per_rank"] = 2 * wl_n
         line["config"]["workload"] += f"_profile_case_{wl_n}"
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only \
+            and args.workload == "zero_bucket":
         line["cpu_baseline"] = cpu_baseline(args)
+    if args.workload == "zero3_per_param":
+        line["config"] = {"workload": "zero3_per_param_k8_h4096_7layer", "K": 8,
+                          "tensors_per_rank": 56, "elements_per_rank": res["wl"].N,
+                          "step": "RS coalesced (ring_fp32, per-parameter shards) + AG coalesced",
+                          "parallelism": "single GPU, 8 simulated ranks",
+                          "l2": "inputs (42 GB resident) far larger than L2; no flush needed"}
+        line["e2e"] = None
     if rank == 0:
         print(json.dumps(line), flush=True)
-    res["wl"].plan.close()
+    if args.workload == "zero3_per_param":
+        res["wl"].close()
+    else:
+        res["wl"].plan.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -8,18 +8,23 @@ all-reduce.  This package is the thin Python binding of those calls.
 """
 from ._binding import (  # noqa: F401
     HOP_BF16,
+    CoalescedPlan,
     LIB_PATH,
     RING_FP32,
     DprError,
     FlattenPlan,
     dpr_allgather,
     dpr_allreduce,
+    dpr_allgather_coalesced,
     dpr_bucket_assign,
+    dpr_coalesced_plan_create,
+    dpr_coalesced_plan_destroy,
     dpr_flatten_bucket,
     dpr_flatten_bucket_noalloc,
     dpr_flatten_plan_create,
     dpr_flatten_plan_destroy,
     dpr_reduce_scatter,
+    dpr_reduce_scatter_coalesced,
     dpr_strerror,
     dpr_version,
     lib,

@@ -38,6 +38,12 @@ _SIGS = {
                           ctypes.POINTER(ctypes.c_int)],
     "dpr_flatten_bucket_noalloc": [ctypes.c_int, ctypes.c_int, _pp, _i64p, _i64p, ctypes.c_int64,
                                    _pp, _c_p],
+    "dpr_coalesced_plan_create": [ctypes.POINTER(_c_p), ctypes.c_int, ctypes.c_int, _pp, _i64p,
+                                  _c_p],
+    "dpr_coalesced_partition_numel": [_c_p, _i64p],
+    "dpr_reduce_scatter_coalesced": [_c_p, _pp, ctypes.c_int, ctypes.c_float, ctypes.c_int, _c_p],
+    "dpr_allgather_coalesced": [_c_p, _pp, _c_p],
+    "dpr_coalesced_plan_destroy": [_c_p],
     "dpr_strerror": [ctypes.c_int],
     "dpr_last_cuda_error": [],
     "dpr_version": [],
@@ -194,6 +200,82 @@ def dpr_flatten_bucket(plan: FlattenPlan, dst: Sequence[torch.Tensor], stream=No
 
 
 def dpr_flatten_plan_destroy(plan: FlattenPlan) -> None:
+    plan.close()
+
+
+class CoalescedPlan:
+    """Owns a dpr_coalesced_plan and keeps its bound tensors alive."""
+
+    def __init__(self, handle: int, K: int, numel: list, partition_numel: int, tensors: list):
+        self.handle = handle
+        self.K = K
+        self.numel = list(numel)
+        self.partition_numel = partition_numel
+        self._tensors = tensors
+
+    def close(self):
+        if self.handle:
+            h, self.handle = self.handle, None
+            _check("dpr_coalesced_plan_destroy", lib().dpr_coalesced_plan_destroy(h))
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dpr_coalesced_plan_create(tensors: Sequence[Sequence[torch.Tensor]], numel: Sequence[int],
+                              stream=None) -> CoalescedPlan:
+    """tensors[r][p]: rank r's tensor of parameter p (bf16, numel[p] elements)."""
+    K, P = len(tensors), len(numel)
+    flat = []
+    for r in range(K):
+        if len(tensors[r]) != P:
+            raise ValueError("every rank needs P tensors")
+        for p in range(P):
+            t = tensors[r][p]
+            if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError("tensors must be contiguous CUDA bf16 tensors")
+            if t.numel() != numel[p]:
+                raise ValueError(f"tensor {p} of rank {r}: {t.numel()} elements, numel says {numel[p]}")
+            flat.append(t)
+    h = ctypes.c_void_p()
+    n_arr = (ctypes.c_int64 * max(P, 1))(*numel)
+    st = lib().dpr_coalesced_plan_create(ctypes.byref(h), K, P, _ptrs(flat), n_arr, _stream(stream))
+    _check("dpr_coalesced_plan_create", st)
+    pn = ctypes.c_int64()
+    _check("dpr_coalesced_partition_numel", lib().dpr_coalesced_partition_numel(h, ctypes.byref(pn)))
+    return CoalescedPlan(h.value, K, numel, pn.value, flat)
+
+
+def dpr_reduce_scatter_coalesced(plan: CoalescedPlan, outputs: Sequence[torch.Tensor],
+                                 mode=RING_FP32, scale: float | None = None,
+                                 accumulate: bool = False, stream=None) -> None:
+    """outputs[j]: rank j's fp32 partition (plan.partition_numel,)."""
+    _need(outputs, plan.K, torch.float32, plan.partition_numel, "outputs")
+    st = lib().dpr_reduce_scatter_coalesced(plan.handle, _ptrs(outputs), _MODES[mode],
+                                            1.0 / plan.K if scale is None else scale,
+                                            int(bool(accumulate)), _stream(stream))
+    _check("dpr_reduce_scatter_coalesced", st)
+
+
+def dpr_allgather_coalesced(plan: CoalescedPlan, shards: Sequence[torch.Tensor],
+                            stream=None) -> None:
+    """shards[j]: rank j's bf16 partition (plan.partition_numel,); writes the
+    plan's bound parameter tensors."""
+    _need(shards, plan.K, torch.bfloat16, plan.partition_numel, "shards")
+    _check("dpr_allgather_coalesced", lib().dpr_allgather_coalesced(plan.handle, _ptrs(shards),
+                                                                    _stream(stream)))
+
+
+def dpr_coalesced_plan_destroy(plan: CoalescedPlan) -> None:
     plan.close()
 
 

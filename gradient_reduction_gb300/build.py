@@ -21,7 +21,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libdpr.so")
-SOURCES = ["dpr_api.cu", "reduce_kernels.cu", "gather_kernels.cu", "flatten_noalloc.cu"]
+SOURCES = ["dpr_api.cu", "reduce_kernels.cu", "gather_kernels.cu", "coalesced.cu",
+           "flatten_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC,-O2",
          "-I", os.path.join(ROOT, "include")]

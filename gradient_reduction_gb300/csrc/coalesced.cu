@@ -1,0 +1,347 @@
+// Per-parameter (ZeRO-3) partitioning: reduce-scatter of fragmented
+// per-parameter gradients into per-parameter shards, and the all-gather that
+// rebuilds full parameters from them.
+//
+// DeepSpeed ZeRO-3 source walkthrough, section 1: each parameter lives as a
+// 1/N shard per rank; section 5.2: the discrete path reduce-scatters the
+// list of fragmented gradients (no flat bucket).  Parameter p of numel n_p is
+// treated as zero-padded to K * s_p, s_p = ceil(n_p / K); rank j owns
+// elements [j*s_p, (j+1)*s_p); rank j's partition buffer holds its shards of
+// every parameter in parameter order (offset_p = sum_{q<p} s_q).  Each shard
+// is the ring-order sum of section 3.2 of the CMU 11-868 Lecture 14 notes,
+// starting at rank j.
+//
+// Work is cut into (parameter, shard) segments and tiles of kCoalTile
+// elements; one block handles one tile (and, for the all-gather, one
+// replica), finding its segment by binary search over first-tile indices.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "dpr_device.cuh"
+#include "dpr_kernels.h"
+#include "dpr_ring.cuh"
+
+namespace dpr {
+namespace {
+
+constexpr int64_t kCoalTile = 4096;     // reduce-scatter tile: K * 8 KB read per block
+constexpr int64_t kCoalAgTile = 8192;   // all-gather tile: 16 KB written per block
+
+struct CoalSeg {
+    int64_t s;        // shard length of the parameter, ceil(n / K)
+    int64_t valid;    // elements of this shard inside the parameter (<= s)
+    int64_t off;      // offset of the parameter's shard in every partition
+    int64_t tile0;    // first reduce-scatter tile of this segment
+    int64_t ag_tile0; // first all-gather tile of this segment
+    int32_t p;        // parameter
+    int32_t j;        // shard (= partition / owning rank)
+    int32_t vec;      // every rank's tensor at j*s is 32-byte aligned, s and off % 16 == 0
+    int32_t pad;
+};
+
+struct CoalParams {
+    const CoalSeg* segs;
+    uint16_t* const* ptrs;          // device table [K * P]: tensors[r * P + p]
+    int64_t n_seg;
+    int64_t n_tiles;
+    float* out[DPR_MAX_RANKS];      // reduce-scatter: fp32 partitions
+    const uint16_t* shard[DPR_MAX_RANKS];   // all-gather: bf16 partitions
+    int K;
+    int P;
+    float scale;
+    int accumulate;
+    int bases_aligned32;            // every out / shard base is 32-byte aligned
+};
+
+template <bool AG>
+__device__ __forceinline__ int64_t find_segment(const CoalSeg* segs, int64_t n_seg, int64_t tile) {
+    int64_t lo = 0, hi = n_seg - 1;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        if ((AG ? segs[mid].ag_tile0 : segs[mid].tile0) <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads) rs_coalesced(const __grid_constant__ CoalParams p) {
+    __shared__ const uint16_t* base[DPR_MAX_RANKS];
+    const int64_t tile = blockIdx.x;
+    const CoalSeg sg = p.segs[find_segment<false>(p.segs, p.n_seg, tile)];
+    const int K = p.K;
+    if (threadIdx.x < K) base[threadIdx.x] = p.ptrs[int64_t(threadIdx.x) * p.P + sg.p] + sg.j * sg.s;
+    __syncthreads();
+    const int64_t t0 = (tile - sg.tile0) * kCoalTile;
+    const int64_t n = (sg.s - t0 < kCoalTile) ? sg.s - t0 : kCoalTile;
+    float* out = p.out[sg.j] + sg.off + t0;
+    if (sg.vec && p.bases_aligned32 && t0 + n <= sg.valid) {
+        // whole tile inside the parameter: 16 elements per thread and access
+        for (int64_t u = threadIdx.x; u < n / 16; u += kThreads) {
+            float acc[16];
+            ring_sum<0, 1, MODE, 8, true>(base, K, sg.j, uint64_t(t0 + 16 * u), acc);
+            store_shard<8>(out + 16 * u, acc, p.scale, p.accumulate);
+        }
+        return;
+    }
+    // element-wise, with the zero padding past the end of the parameter
+    for (int64_t i = threadIdx.x; i < n; i += kThreads) {
+        const int64_t e = t0 + i;
+        const bool in = e < sg.valid;
+        float acc = 0.0f;
+        uint16_t hop = 0;
+        for (int k = 0; k < K; ++k) {
+            int r = sg.j + k;
+            r = (r >= K) ? r - K : r;
+            const uint16_t x = in ? base[r][e] : uint16_t(0);
+            if constexpr (MODE == DPR_SUM_RING_FP32) acc = (k == 0) ? bf_1(x) : __fadd_rn(acc, bf_1(x));
+            else hop = (k == 0) ? x : add_bf16(hop, x);
+        }
+        if constexpr (MODE == DPR_SUM_HOP_BF16) acc = bf_1(hop);
+        float v = __fmul_rn(acc, p.scale);
+        if (p.accumulate) v = __fadd_rn(out[i], v);
+        out[i] = v;
+    }
+}
+
+// One block per (tile, replica r); the K replicas of a tile are adjacent so
+// the shard tile is read from HBM once.  Only the shard's elements inside the
+// parameter are written (padding is dropped).
+__global__ void __launch_bounds__(kThreads) ag_coalesced(const __grid_constant__ CoalParams p) {
+    const uint64_t b = blockIdx.x;
+    const int r = int(b % uint64_t(p.K));
+    const int64_t tile = int64_t(b / uint64_t(p.K));
+    const CoalSeg sg = p.segs[find_segment<true>(p.segs, p.n_seg, tile)];
+    const int64_t t0 = (tile - sg.ag_tile0) * kCoalAgTile;
+    const int64_t n = (sg.valid - t0 < kCoalAgTile) ? sg.valid - t0 : kCoalAgTile;
+    if (n <= 0) return;
+    const uint16_t* src = p.shard[sg.j] + sg.off + t0;
+    uint16_t* dst = p.ptrs[int64_t(r) * p.P + sg.p] + sg.j * sg.s + t0;
+    if (sg.vec && p.bases_aligned32 && n == kCoalAgTile) {
+#pragma unroll
+        for (int u = 0; u < int(kCoalAgTile) / 16 / kThreads; ++u) {
+            const int i = (u * kThreads + int(threadIdx.x)) * 16;
+            uint32_t w[8];
+            load_words<8, true>(src + i, w);
+            store_words<8>(dst + i, w);
+        }
+        return;
+    }
+    for (int64_t i = threadIdx.x; i < n; i += kThreads) dst[i] = src[i];
+}
+
+struct Span {
+    uintptr_t lo, hi;
+};
+
+bool overlap(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned_to(const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; }
+
+dpr_status coal_cuda(cudaError_t e) { return record_cuda_status(e); }
+
+}  // namespace
+}  // namespace dpr
+
+using namespace dpr;
+
+struct dpr_coalesced_plan {
+    int K = 0;
+    int P = 0;
+    int device = 0;
+    int64_t partition_numel = 0;
+    int64_t n_tiles = 0;
+    int64_t n_ag_tiles = 0;
+    std::vector<int64_t> numel;
+    std::vector<CoalSeg> segs;
+    std::vector<Span> tensor_spans;
+    CoalSeg* d_segs = nullptr;
+    uint16_t** d_ptrs = nullptr;
+};
+
+extern "C" {
+
+dpr_status dpr_coalesced_plan_create(dpr_coalesced_plan** plan, int K, int P,
+                                     void* const* tensors, const int64_t* numel, void* stream) {
+    if (!plan) return DPR_ERR_INVALID_ARG;
+    *plan = nullptr;
+    if (K < 2 || K > DPR_MAX_RANKS || P < 0) return DPR_ERR_INVALID_ARG;
+    if (P > 0 && (!tensors || !numel)) return DPR_ERR_INVALID_ARG;
+    std::vector<Span> spans;
+    for (int p = 0; p < P; ++p) {
+        if (numel[p] < 0) return DPR_ERR_INVALID_ARG;
+        if (numel[p] > DPR_MAX_ELEMS) return DPR_ERR_UNSUPPORTED;
+        for (int r = 0; r < K; ++r) {
+            const void* t = tensors[size_t(r) * P + p];
+            if (numel[p] == 0) continue;
+            if (!t) return DPR_ERR_INVALID_ARG;
+            if (!aligned_to(t, 2)) return DPR_ERR_ALIGNMENT;
+            const uintptr_t a = reinterpret_cast<uintptr_t>(t);
+            spans.push_back(Span{a, a + uintptr_t(numel[p]) * 2});
+        }
+    }
+    // the all-gather writes these tensors: they must not overlap
+    std::vector<Span> sorted = spans;
+    std::sort(sorted.begin(), sorted.end(), [](const Span& a, const Span& b) { return a.lo < b.lo; });
+    for (size_t i = 1; i < sorted.size(); ++i)
+        if (sorted[i].lo < sorted[i - 1].hi) return DPR_ERR_ALIAS;
+
+    dpr_coalesced_plan* pl = new (std::nothrow) dpr_coalesced_plan();
+    if (!pl) return DPR_ERR_CUDA;
+    pl->K = K;
+    pl->P = P;
+    pl->numel.assign(numel, numel + P);
+    pl->tensor_spans = spans;
+    int64_t off = 0, tiles = 0, ag_tiles = 0;
+    for (int p = 0; p < P; ++p) {
+        const int64_t s = (numel[p] + K - 1) / K;
+        if (s == 0) continue;
+        for (int j = 0; j < K; ++j) {
+            CoalSeg g;
+            g.s = s;
+            g.valid = std::max<int64_t>(0, std::min<int64_t>(s, numel[p] - int64_t(j) * s));
+            g.off = off;
+            g.tile0 = tiles;
+            g.ag_tile0 = ag_tiles;
+            g.p = p;
+            g.j = j;
+            bool vec = (s % 16 == 0) && (off % 16 == 0);
+            for (int r = 0; r < K && vec; ++r)
+                vec = aligned_to(static_cast<const uint16_t*>(tensors[size_t(r) * P + p]) + j * s, 32);
+            g.vec = vec ? 1 : 0;
+            g.pad = 0;
+            tiles += (s + kCoalTile - 1) / kCoalTile;
+            ag_tiles += (s + kCoalAgTile - 1) / kCoalAgTile;
+            pl->segs.push_back(g);
+        }
+        off += s;
+    }
+    pl->partition_numel = off;
+    pl->n_tiles = tiles;
+    pl->n_ag_tiles = ag_tiles;
+    cudaError_t e = cudaGetDevice(&pl->device);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (e == cudaSuccess && !pl->segs.empty()) {
+        e = cudaMalloc(reinterpret_cast<void**>(&pl->d_segs), pl->segs.size() * sizeof(CoalSeg));
+        if (e == cudaSuccess)
+            e = cudaMalloc(reinterpret_cast<void**>(&pl->d_ptrs), size_t(K) * P * sizeof(uint16_t*));
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(pl->d_segs, pl->segs.data(), pl->segs.size() * sizeof(CoalSeg),
+                                cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(pl->d_ptrs, tensors, size_t(K) * P * sizeof(uint16_t*),
+                                cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    if (e != cudaSuccess) {
+        if (pl->d_segs) cudaFree(pl->d_segs);
+        if (pl->d_ptrs) cudaFree(pl->d_ptrs);
+        delete pl;
+        return coal_cuda(e);
+    }
+    *plan = pl;
+    return DPR_OK;
+}
+
+dpr_status dpr_coalesced_partition_numel(const dpr_coalesced_plan* plan, int64_t* numel) {
+    if (!plan || !numel) return DPR_ERR_INVALID_ARG;
+    *numel = plan->partition_numel;
+    return DPR_OK;
+}
+
+dpr_status dpr_reduce_scatter_coalesced(const dpr_coalesced_plan* plan, float* const* out,
+                                        int mode, float scale, int accumulate, void* stream) {
+    if (!plan || !out) return DPR_ERR_INVALID_ARG;
+    if (mode != DPR_SUM_RING_FP32 && mode != DPR_SUM_HOP_BF16) return DPR_ERR_INVALID_ARG;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return coal_cuda(e);
+    if (dev != plan->device) return DPR_ERR_INVALID_ARG;
+    const int K = plan->K;
+    bool a32 = true;
+    std::vector<Span> outs;
+    for (int j = 0; j < K; ++j) {
+        if (!out[j]) return DPR_ERR_INVALID_ARG;
+        if (!aligned_to(out[j], 4)) return DPR_ERR_ALIGNMENT;
+        a32 = a32 && aligned_to(out[j], 32);
+        const uintptr_t a = reinterpret_cast<uintptr_t>(out[j]);
+        outs.push_back(Span{a, a + uintptr_t(plan->partition_numel) * 4});
+    }
+    for (int j = 0; j < K; ++j)
+        for (int q = j + 1; q < K; ++q)
+            if (overlap(outs[j], outs[q])) return DPR_ERR_ALIAS;
+    for (const Span& t : plan->tensor_spans)
+        for (const Span& o : outs)
+            if (overlap(t, o)) return DPR_ERR_ALIAS;
+    if (plan->n_tiles == 0) return DPR_OK;
+    CoalParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.segs = plan->d_segs;
+    prm.ptrs = plan->d_ptrs;
+    prm.n_seg = int64_t(plan->segs.size());
+    prm.n_tiles = plan->n_tiles;
+    for (int j = 0; j < K; ++j) prm.out[j] = out[j];
+    prm.K = K;
+    prm.P = plan->P;
+    prm.scale = scale;
+    prm.accumulate = accumulate ? 1 : 0;
+    prm.bases_aligned32 = a32 ? 1 : 0;
+    const void* k = (mode == DPR_SUM_RING_FP32)
+                        ? reinterpret_cast<const void*>(rs_coalesced<DPR_SUM_RING_FP32>)
+                        : reinterpret_cast<const void*>(rs_coalesced<DPR_SUM_HOP_BF16>);
+    void* args[] = {&prm};
+    return coal_cuda(cudaLaunchKernel(k, dim3(unsigned(plan->n_tiles)), dim3(kThreads), args, 0,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+dpr_status dpr_allgather_coalesced(const dpr_coalesced_plan* plan, const void* const* shards,
+                                   void* stream) {
+    if (!plan || !shards) return DPR_ERR_INVALID_ARG;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return coal_cuda(e);
+    if (dev != plan->device) return DPR_ERR_INVALID_ARG;
+    const int K = plan->K;
+    bool a32 = true;
+    for (int j = 0; j < K; ++j) {
+        if (!shards[j]) return DPR_ERR_INVALID_ARG;
+        if (!aligned_to(shards[j], 2)) return DPR_ERR_ALIGNMENT;
+        a32 = a32 && aligned_to(shards[j], 32);
+        const uintptr_t a = reinterpret_cast<uintptr_t>(shards[j]);
+        const Span sp{a, a + uintptr_t(plan->partition_numel) * 2};
+        for (const Span& t : plan->tensor_spans)
+            if (overlap(t, sp)) return DPR_ERR_ALIAS;
+    }
+    if (plan->n_tiles == 0) return DPR_OK;
+    CoalParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.segs = plan->d_segs;
+    prm.ptrs = plan->d_ptrs;
+    prm.n_seg = int64_t(plan->segs.size());
+    prm.n_tiles = plan->n_tiles;
+    for (int j = 0; j < K; ++j) prm.shard[j] = static_cast<const uint16_t*>(shards[j]);
+    prm.K = K;
+    prm.P = plan->P;
+    prm.bases_aligned32 = a32 ? 1 : 0;
+    const uint64_t blocks = uint64_t(plan->n_ag_tiles) * uint64_t(K);
+    void* args[] = {&prm};
+    return coal_cuda(cudaLaunchKernel(reinterpret_cast<const void*>(ag_coalesced),
+                                      dim3(unsigned(blocks)), dim3(kThreads), args, 0,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+dpr_status dpr_coalesced_plan_destroy(dpr_coalesced_plan* plan) {
+    if (!plan) return DPR_OK;
+    cudaError_t e = cudaSuccess;
+    if (plan->d_segs) e = cudaFree(plan->d_segs);
+    if (plan->d_ptrs) {
+        cudaError_t e2 = cudaFree(plan->d_ptrs);
+        if (e == cudaSuccess) e = e2;
+    }
+    delete plan;
+    return coal_cuda(e);
+}
+
+}  // extern "C"

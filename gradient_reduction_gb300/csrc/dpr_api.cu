@@ -22,6 +22,12 @@ dpr_status cuda_status(cudaError_t e) {
     return DPR_ERR_CUDA;
 }
 
+}  // namespace
+
+dpr_status record_cuda_status(cudaError_t e) { return cuda_status(e); }
+
+namespace {
+
 struct Span {
     uintptr_t lo, hi;  // [lo, hi)
 };

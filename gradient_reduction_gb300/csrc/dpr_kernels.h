@@ -80,6 +80,10 @@ cudaError_t launch_allreduce(const ArParams& p, int mode, int width, cudaStream_
 cudaError_t launch_allgather(const AgParams& p, int width, cudaStream_t s);
 cudaError_t launch_flatten(const FlatParams& p, cudaStream_t s);
 
+// Maps a CUDA result to a status, remembering a failure for
+// dpr_last_cuda_error() (per calling thread).
+dpr_status record_cuda_status(cudaError_t e);
+
 // Grid helper: blocks per chunk so that K chunks together fill the GPU with
 // `blocks_per_sm` resident blocks per SM, and no more blocks than there is work.
 cudaError_t blocks_per_chunk(const void* kernel, int K, uint64_t work_per_chunk, int* gx);

@@ -190,6 +190,50 @@ dpr_status dpr_flatten_bucket_noalloc(int K, int P, const void* const* src, cons
                                       void* const* dst, void* stream);
 
 /*
+ * Per-parameter partitioning (ZeRO-3): the discrete reduction path and the
+ * parameter all-gather.  DeepSpeed ZeRO-3 source walkthrough, section 1:
+ * every parameter lives as a 1/N shard per rank; section 5.2: with
+ * fragmented gradients the list of per-parameter gradients is
+ * reduce-scattered directly, without a flat bucket.
+ *
+ * Layout: parameter p of numel[p] elements is treated as zero-padded to
+ * K * s_p, s_p = ceil(numel[p] / K); rank j owns elements [j*s_p, (j+1)*s_p).
+ * Rank j's partition buffer holds its shards of all parameters in parameter
+ * order: the shard of p starts at offset_p = s_0 + ... + s_{p-1}, and the
+ * partition holds dpr_coalesced_partition_numel() elements.
+ *
+ * dpr_coalesced_plan_create binds the K*P per-rank tensors (gradients for the
+ * reduce-scatter, parameters for the all-gather; tensors[r*P + p] = rank r's
+ * tensor of parameter p, bf16, numel[p] elements, non-overlapping) and
+ * uploads a segment table and the pointer table once (cudaMalloc; waits for
+ * the upload).  numel[p] == 0 is allowed.
+ *
+ * dpr_reduce_scatter_coalesced: out[j][offset_p + t] = scale * (ring-order
+ * sum over ranks, starting at rank j, of tensors[r*P + p][j*s_p + t]), padding
+ * summing to zero; mode, scale and accumulate as in dpr_reduce_scatter
+ * (one micro-batch).  out: host array [K] of fp32 partition buffers, not
+ * overlapping each other or the bound tensors.
+ *
+ * dpr_allgather_coalesced: tensors[r*P + p][j*s_p + t] = shards[j][offset_p + t]
+ * for every r, j and every t with j*s_p + t < numel[p] (padding dropped).
+ * shards: host array [K] of bf16 partition buffers, not overlapping the bound
+ * tensors.
+ *
+ * Each call launches one kernel on `stream`; plan destruction frees the
+ * tables and synchronises the device.
+ */
+typedef struct dpr_coalesced_plan dpr_coalesced_plan;
+
+dpr_status dpr_coalesced_plan_create(dpr_coalesced_plan** plan, int K, int P, void* const* tensors,
+                                     const int64_t* numel, void* stream);
+dpr_status dpr_coalesced_partition_numel(const dpr_coalesced_plan* plan, int64_t* numel);
+dpr_status dpr_reduce_scatter_coalesced(const dpr_coalesced_plan* plan, float* const* out, int mode,
+                                        float scale, int accumulate, void* stream);
+dpr_status dpr_allgather_coalesced(const dpr_coalesced_plan* plan, const void* const* shards,
+                                   void* stream);
+dpr_status dpr_coalesced_plan_destroy(dpr_coalesced_plan* plan);
+
+/*
  * Bucket formation, host only (DeepSpeed ZeRO-3 source walkthrough, sections
  * 3.1, 5.1, 5.4): gradients in arrival order are appended at the running
  * offset; the bucket is flushed first when adding the next gradient would

@@ -219,3 +219,66 @@ def allreduce(x: list, K: int, mode: int = RING_FP32, scale: float = 1.0,
         wire.append(w)
     _ag_rounds(wire, K, S, 1, ctr, trace)
     return wire, ctr
+
+
+# ---- per-parameter partitioning (ZeRO-3) -----------------------------------------
+#
+# DeepSpeed ZeRO-3 source walkthrough, section 1: every parameter lives as a
+# 1/N shard (ds_tensor) per rank; section 5.2: when gradients stay fragmented,
+# the discrete path reduce-scatters the list of per-parameter gradients, so
+# each rank receives its shard of every gradient.  Reading: parameter p of
+# numel n_p is padded with zeros to K * s_p, s_p = ceil(n_p / K), and rank j
+# owns elements [j * s_p, (j + 1) * s_p); a rank's partition buffer holds its
+# shards of all parameters in parameter order.
+
+def shard_layout(numel: list, K: int):
+    """(s_p, offset_p) per parameter and the partition length sum_p s_p."""
+    sizes = [-(-int(n) // K) for n in numel]
+    offs, o = [], 0
+    for s in sizes:
+        offs.append(o)
+        o += s
+    return sizes, offs, o
+
+
+def _padded(a, total: int) -> np.ndarray:
+    out = np.zeros(total, dtype=np.uint16)
+    out[:len(a)] = np.asarray(a, dtype=np.uint16)
+    return out
+
+
+def reduce_scatter_coalesced(grads: list, numel: list, K: int, mode: int = RING_FP32,
+                             scale: float = 1.0, out_init: list | None = None):
+    """grads[r][p]: rank r's gradient of parameter p (uint16 bf16 bits, numel[p]).
+    Returns K float32 partition buffers: partition j = concatenation over p of
+    the ring reduce-scatter's shard j of parameter p (padding included)."""
+    sizes, offs, total = shard_layout(numel, K)
+    parts = [np.zeros(total, dtype=np.float32) if out_init is None
+             else np.asarray(out_init[j], dtype=np.float32).copy() for j in range(K)]
+    for p, (s, o) in enumerate(zip(sizes, offs)):
+        if s == 0:
+            continue
+        x = [_padded(grads[r][p], K * s) for r in range(K)]
+        init = None if out_init is None else [parts[j][o:o + s] for j in range(K)]
+        shards, _ = reduce_scatter(x, K, 1, mode, scale, out_init=init)
+        for j in range(K):
+            parts[j][o:o + s] = shards[j]
+    return parts
+
+
+def allgather_coalesced(partitions: list, numel: list, K: int) -> list:
+    """partitions[j]: rank j's bf16 shard partition (uint16, sum_p s_p).
+    Returns params[r][p] (uint16, numel[p]): the ring all-gather of every
+    parameter's shards, padding dropped."""
+    sizes, offs, _ = shard_layout(numel, K)
+    params = [[None] * len(numel) for _ in range(K)]
+    for p, (n, s, o) in enumerate(zip(numel, sizes, offs)):
+        if s == 0:
+            for r in range(K):
+                params[r][p] = np.zeros(0, dtype=np.uint16)
+            continue
+        outs, _ = allgather([np.asarray(partitions[j], dtype=np.uint16)[o:o + s]
+                             for j in range(K)], K)
+        for r in range(K):
+            params[r][p] = outs[r][:n].copy()
+    return params

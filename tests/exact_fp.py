@@ -8,7 +8,7 @@ e = emin).  round_to() returns the nearest such value to a Fraction, ties to the
 even significand, and +-inf past the largest finite value (IEEE 754 section 4.3.1,
 roundTiesToEven).
 """
-from fractions import Fraction
+from fractions import Fraction  # noqa: F401  (re-exported for tests)
 import math
 import struct
 

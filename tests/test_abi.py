@@ -35,7 +35,7 @@ def _declared():
 
 def test_exports_every_declared_function(L):
     names = _declared()
-    assert len(names) == 11
+    assert len(names) == 16
     for n in names:
         assert hasattr(L, n), n
 
@@ -163,3 +163,18 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _binding.lib()
+
+
+def test_coalesced_rejections(L):
+    h = ctypes.c_void_p()
+    n = (ctypes.c_int64 * 2)(64, 64)
+    t = _arr(_bufs(4, 1 << 20))
+    assert L.dpr_coalesced_plan_create(ctypes.byref(h), 1, 2, t, n, None) == INVALID     # K < 2
+    over = _arr([BASE, BASE + 64, BASE + (1 << 20), BASE + (2 << 20)])                   # tensors overlap
+    assert L.dpr_coalesced_plan_create(ctypes.byref(h), 2, 2, over, n, None) == ALIAS
+    odd = _arr([BASE + 1, BASE + (1 << 20), BASE + (2 << 20), BASE + (3 << 20)])
+    assert L.dpr_coalesced_plan_create(ctypes.byref(h), 2, 2, odd, n, None) == ALIGN
+    assert h.value is None
+    assert L.dpr_reduce_scatter_coalesced(None, None, 0, 1.0, 0, None) == INVALID
+    assert L.dpr_allgather_coalesced(None, None, None) == INVALID
+    assert L.dpr_coalesced_plan_destroy(None) == OK
