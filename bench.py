@@ -76,9 +76,11 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
-    p.add_argument("--workload", choices=["zero_bucket", "zero3_per_param"], default="zero_bucket",
+    p.add_argument("--workload", choices=["zero_bucket", "zero3_per_param", "bucket_pipeline"],
+                   default="zero_bucket",
                    help="zero_bucket: the headline step (default); zero3_per_param: the ZeRO-3 "
-                        "discrete path on config 3's 56 gradients")
+                        "discrete path on config 3's 56 gradients; bucket_pipeline: backward "
+                        "time under the stream-overlap policies")
     p.add_argument("--only", choices=STEP_KERNELS + Z3_KERNELS, default=None,
                    help="profile helper: launch only this kernel per step")
     p.add_argument("--n-per-rank", type=int, default=None,
@@ -346,6 +348,142 @@ class Zero3Workload:
         self.ag_plan.close()
 
 
+class PipelineBackward:
+    """A simulated backward pass for the bucket pipeline: 16 buckets (one
+    gradient per rank each, K=8, alternately 3 * 2**23 and 2**23 elements),
+    each preceded by backward compute stood in for by bf16 4096^3 matmuls on
+    the compute stream (alternately 1 and 3), so the reductions of large
+    buckets outlast the compute that follows them.  run() times one backward
+    under a wait policy ("per_buffer", "reverse_wait") or "serial" (gather and
+    reduce on the compute stream, i.e. no overlap)."""
+
+    def __init__(self, dev, n_buckets=16):
+        import torch
+        import gradient_reduction_gb300 as dpr
+        from workloads import synthetic as syn
+        self.torch, self.dpr, self.dev = torch, dpr, dev
+        self.K = K = 8
+        self.sizes = [3 * (1 << 23) if i % 2 == 0 else (1 << 23) for i in range(n_buckets)]
+        self.mms = [1 if i % 2 == 0 else 3 for i in range(n_buckets)]
+        self.grads = [[syn.gauss_bf16(0, n, syn.stream_key(0x91, r, 0, i), 1e-3, device=dev)
+                       for r in range(K)] for i, n in enumerate(self.sizes)]
+        self.plans = [dpr.dpr_flatten_plan_create([[g] for g in gi], [n], [0], n)
+                      for gi, n in zip(self.grads, self.sizes)]
+        self.outs = [[torch.empty(n // K, dtype=torch.float32, device=dev) for _ in range(K)]
+                     for n in self.sizes]
+        self.a = torch.randn(4096, 4096, device=dev).to(torch.bfloat16)
+        self.b = torch.randn(4096, 4096, device=dev).to(torch.bfloat16)
+        self.c = torch.empty(4096, 4096, dtype=torch.bfloat16, device=dev)
+        self.ipg = [torch.empty(max(self.sizes), dtype=torch.bfloat16, device=dev) for _ in range(K)]
+        self.bytes = sum(4 * K * n + 2 * K * n + 4 * n for n in self.sizes)   # gather + RS
+        self.cur = torch.cuda.Stream(device=dev)
+        torch.cuda.synchronize()
+
+    def compute(self, i):
+        for _ in range(self.mms[i]):
+            self.torch.matmul(self.a, self.b, out=self.c)
+
+    def run(self, policy: str, max_blocks: int = 0) -> float:
+        torch, dpr, K = self.torch, self.dpr, self.K
+        cur = self.cur
+        pipe = None
+        if policy != "serial":
+            pipe = dpr.BucketPipeline(K, max(self.sizes), 2,
+                                      dpr.WAIT_PER_BUFFER if policy == "per_buffer"
+                                      else dpr.WAIT_REDUCTION_STREAM, max_blocks)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(cur):
+            t0.record(cur)
+            for i, n in enumerate(self.sizes):
+                self.compute(i)
+                if pipe is None:
+                    views = [t[:n] for t in self.ipg]
+                    dpr.dpr_flatten_bucket(self.plans[i], views, stream=cur)
+                    dpr.dpr_reduce_scatter(views, K, 1, n, self.outs[i], stream=cur)
+                else:
+                    pipe.submit(self.plans[i], self.outs[i], stream=cur)
+            if pipe is not None:
+                pipe.flush(stream=cur)
+            t1.record(cur)
+        torch.cuda.synchronize()
+        if pipe is not None:
+            pipe.close()
+        return t0.elapsed_time(t1) / 1e3
+
+    def run_parts(self):
+        """Compute alone and gather+reduce alone (serial), for the overlap bound."""
+        torch, dpr, K, cur = self.torch, self.dpr, self.K, self.cur
+        res = {}
+        for name in ("compute", "reduce"):
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(cur):
+                t0.record(cur)
+                for i, n in enumerate(self.sizes):
+                    if name == "compute":
+                        self.compute(i)
+                    else:
+                        views = [t[:n] for t in self.ipg]
+                        dpr.dpr_flatten_bucket(self.plans[i], views, stream=cur)
+                        dpr.dpr_reduce_scatter(views, K, 1, n, self.outs[i], stream=cur)
+                t1.record(cur)
+            torch.cuda.synchronize()
+            res[name] = t0.elapsed_time(t1) / 1e3
+        return res
+
+    def close(self):
+        for p in self.plans:
+            p.close()
+
+
+def run_pipeline_bench(args):
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pb = PipelineBackward(dev)
+    budgets = (0, 608, 304, 152, 64)
+    keys = ["serial"] + [f"{pol}@{mb}" for mb in budgets for pol in ("reverse_wait", "per_buffer")]
+
+    def run(key):
+        if key == "serial":
+            return pb.run("serial")
+        pol, mb = key.split("@")
+        return pb.run(pol, int(mb))
+    for key in keys:
+        for _ in range(args.warmup):
+            run(key)
+    times = {key: [] for key in keys}
+    for _ in range(args.steps):
+        for key in keys:
+            times[key].append(run(key))
+    med = {key: statistics.median(v) for key, v in times.items()}
+    parts = pb.run_parts()
+    pb.close()
+    best = min((k for k in keys if k.startswith("per_buffer")), key=lambda k: med[k])
+    mb = best.split("@")[1]
+    med["per_buffer"] = med[best]
+    med["reverse_wait"] = med[f"reverse_wait@{mb}"]
+    line = {
+        "metric": "bucket pipeline: simulated backward time per policy", "unit": "ms",
+        "value": round(med["per_buffer"] * 1e3, 3), "higher_is_better": False,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "config": {"workload": "bucket_pipeline_k8_16_buckets",
+                   "buckets": "16, alternately 3*2^23 and 2^23 bf16 elements per rank, K=8",
+                   "compute": "bf16 4096^3 matmuls on the compute stream, alternately 1 and 3 per bucket",
+                   "buffers": 2},
+        "ms": {k: round(v * 1e3, 3) for k, v in med.items()},
+        "reduction_block_budget": int(mb),
+        "alone_ms": {k: round(v * 1e3, 3) for k, v in parts.items()},
+        "gather_reduce_gbs_serial": round(pb.bytes / parts["reduce"] / 1e9, 1),
+        "per_buffer_vs_reverse_wait": round(med["reverse_wait"] / med["per_buffer"], 3),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_device(args, rank, world, local_rank):
     import torch
     dev = torch.device("cuda", local_rank)
@@ -572,6 +710,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "bucket_pipeline":
+        return run_pipeline_bench(args)
     import torch
     rank, world, local_rank = dist_env()
     if world > 1:

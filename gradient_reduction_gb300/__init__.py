@@ -7,6 +7,9 @@ with averaging and the fp32 partition cast, the all-gather and the fused
 all-reduce.  This package is the thin Python binding of those calls.
 """
 from ._binding import (  # noqa: F401
+    WAIT_PER_BUFFER,
+    WAIT_REDUCTION_STREAM,
+    BucketPipeline,
     HOP_BF16,
     CoalescedPlan,
     LIB_PATH,

@@ -44,6 +44,13 @@ _SIGS = {
     "dpr_reduce_scatter_coalesced": [_c_p, _pp, ctypes.c_int, ctypes.c_float, ctypes.c_int, _c_p],
     "dpr_allgather_coalesced": [_c_p, _pp, _c_p],
     "dpr_coalesced_plan_destroy": [_c_p],
+    "dpr_bucket_pipeline_create": [ctypes.POINTER(_c_p), ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int],
+    "dpr_bucket_pipeline_submit": [_c_p, _c_p, _pp, ctypes.c_int, ctypes.c_float, ctypes.c_int, _pp,
+                                   ctypes.c_int, _c_p],
+    "dpr_bucket_pipeline_flush": [_c_p, _c_p],
+    "dpr_bucket_pipeline_stream": [_c_p, ctypes.POINTER(_c_p)],
+    "dpr_bucket_pipeline_destroy": [_c_p],
     "dpr_strerror": [ctypes.c_int],
     "dpr_last_cuda_error": [],
     "dpr_version": [],
@@ -277,6 +284,63 @@ def dpr_allgather_coalesced(plan: CoalescedPlan, shards: Sequence[torch.Tensor],
 
 def dpr_coalesced_plan_destroy(plan: CoalescedPlan) -> None:
     plan.close()
+
+
+WAIT_PER_BUFFER = 0
+WAIT_REDUCTION_STREAM = 1
+
+
+class BucketPipeline:
+    """Owns a dpr_bucket_pipeline; keeps each submitted bucket's plan and
+    outputs alive until the pipeline is flushed or closed."""
+
+    def __init__(self, K: int, bucket_capacity: int, n_buffers: int = 2,
+                 wait_policy: int = WAIT_PER_BUFFER, max_blocks: int = 0):
+        h = ctypes.c_void_p()
+        _check("dpr_bucket_pipeline_create",
+               lib().dpr_bucket_pipeline_create(ctypes.byref(h), K, bucket_capacity, n_buffers,
+                                                wait_policy, max_blocks))
+        self.handle, self.K = h.value, K
+        self._keep = []
+
+    def submit(self, plan: FlattenPlan, outputs: Sequence[torch.Tensor], mode=RING_FP32,
+               scale: float | None = None, accumulate: bool = False, producers=(), stream=None):
+        _need(outputs, self.K, torch.float32, plan.bucket_numel // self.K, "outputs")
+        prod = [_stream(p) for p in producers]
+        parr = (ctypes.c_void_p * max(len(prod), 1))(*prod)
+        st = lib().dpr_bucket_pipeline_submit(self.handle, plan.handle, _ptrs(outputs), _MODES[mode],
+                                              1.0 / self.K if scale is None else scale,
+                                              int(bool(accumulate)), parr, len(prod),
+                                              _stream(stream))
+        _check("dpr_bucket_pipeline_submit", st)
+        self._keep.append((plan, list(outputs)))
+
+    def reduction_stream(self) -> torch.cuda.ExternalStream:
+        """The pipeline's reduction stream, for ordering or timing other work."""
+        h = ctypes.c_void_p()
+        _check("dpr_bucket_pipeline_stream", lib().dpr_bucket_pipeline_stream(self.handle, ctypes.byref(h)))
+        return torch.cuda.ExternalStream(h.value)
+
+    def flush(self, stream=None):
+        _check("dpr_bucket_pipeline_flush", lib().dpr_bucket_pipeline_flush(self.handle, _stream(stream)))
+
+    def close(self):
+        if self.handle:
+            h, self.handle = self.handle, None
+            _check("dpr_bucket_pipeline_destroy", lib().dpr_bucket_pipeline_destroy(h))
+            self._keep = []
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def dpr_flatten_bucket_noalloc(srcs: Sequence[Sequence[torch.Tensor]], numel: Sequence[int],

@@ -107,20 +107,20 @@ cudaError_t blocks_per_chunk(const void* kernel, int K, uint64_t work_per_chunk,
 
 using namespace dpr;
 
-struct dpr_flatten_plan {
-    int K = 0;
-    int P = 0;
-    int device = 0;
-    int64_t bucket_numel = 0;
-    int64_t n_tiles = 0;
-    std::vector<FlatSeg> segs;     // host copy
-    FlatSeg* d_segs = nullptr;     // device copy
-};
 
 extern "C" {
 
 dpr_status dpr_reduce_scatter(const void* const* in, int K, int M, int64_t N, float* const* out,
                               int mode, float scale, int accumulate, void* stream) {
+    return dpr::reduce_scatter_capped(in, K, M, N, out, mode, scale, accumulate,
+                                      static_cast<cudaStream_t>(stream), 0);
+}
+
+}  // extern "C"
+
+dpr_status dpr::reduce_scatter_capped(const void* const* in, int K, int M, int64_t N,
+                                      float* const* out, int mode, float scale, int accumulate,
+                                      cudaStream_t stream, int max_blocks) {
     dpr_status st = check_kn(K, N);
     if (st != DPR_OK) return st;
     if (M < 1 || M > DPR_MAX_MICRO) return DPR_ERR_INVALID_ARG;
@@ -160,8 +160,10 @@ dpr_status dpr_reduce_scatter(const void* const* in, int K, int M, int64_t N, fl
     p.M = M;
     p.scale = scale;
     p.accumulate = accumulate ? 1 : 0;
-    return cuda_status(launch_reduce_scatter(p, mode, width, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_reduce_scatter(p, mode, width, stream, max_blocks));
 }
+
+extern "C" {
 
 dpr_status dpr_allgather(const void* const* shard, int K, int64_t N, void* const* out,
                          void* stream) {

@@ -6,6 +6,8 @@
 #pragma once
 
 #include <cstdint>
+#include <vector>
+
 #include <cuda_runtime.h>
 
 #include "../../include/dpr.h"
@@ -75,7 +77,14 @@ inline int access_width(int64_t S, bool aligned32, bool aligned16) {
 
 // Launchers: return cudaSuccess or the launch error.  `width` as above;
 // RsParams::su / ArParams::su hold S / (2 * width) when width > 0.
-cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaStream_t s);
+// max_blocks > 0 caps the grid at about that many blocks (grid-stride).
+cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaStream_t s,
+                                  int max_blocks = 0);
+
+// dpr_reduce_scatter with a block budget (0 = the whole GPU).
+dpr_status reduce_scatter_capped(const void* const* in, int K, int M, int64_t N, float* const* out,
+                                 int mode, float scale, int accumulate, cudaStream_t stream,
+                                 int max_blocks);
 cudaError_t launch_allreduce(const ArParams& p, int mode, int width, cudaStream_t s);
 cudaError_t launch_allgather(const AgParams& p, int width, cudaStream_t s);
 cudaError_t launch_flatten(const FlatParams& p, cudaStream_t s);
@@ -89,3 +98,15 @@ dpr_status record_cuda_status(cudaError_t e);
 cudaError_t blocks_per_chunk(const void* kernel, int K, uint64_t work_per_chunk, int* gx);
 
 }  // namespace dpr
+
+// A flatten plan (see dpr_flatten_plan_create): the host and device copies of
+// its segment table.
+struct dpr_flatten_plan {
+    int K = 0;
+    int P = 0;
+    int device = 0;
+    int64_t bucket_numel = 0;
+    int64_t n_tiles = 0;
+    std::vector<dpr::FlatSeg> segs;     // host copy
+    dpr::FlatSeg* d_segs = nullptr;     // device copy
+};

@@ -26,15 +26,19 @@ namespace {
 
 // ---- reduce-scatter ------------------------------------------------------------
 
+// One unit per thread when the grid covers the chunk (the default launch);
+// with a capped grid (a block budget, e.g. to leave SMs to concurrent
+// compute) the same blocks stride over the remaining units.
 template <int KC, int M, int MODE, int W>
 __global__ void __launch_bounds__(kThreads) rs_vec(const __grid_constant__ RsParams p) {
-    const uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x;
-    if (t >= p.su) return;
     const int j = blockIdx.y;
-    const uint64_t e = uint64_t(j) * uint64_t(p.S) + uint64_t(2 * W) * t;
-    float acc[2 * W];
-    ring_sum<KC, M, MODE, W, true>(p.in, p.K, j, e, acc);
-    store_shard<W>(p.out[j] + uint64_t(2 * W) * t, acc, p.scale, p.accumulate);
+    for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < p.su;
+         t += uint64_t(gridDim.x) * kThreads) {
+        const uint64_t e = uint64_t(j) * uint64_t(p.S) + uint64_t(2 * W) * t;
+        float acc[2 * W];
+        ring_sum<KC, M, MODE, W, true>(p.in, p.K, j, e, acc);
+        store_shard<W>(p.out[j] + uint64_t(2 * W) * t, acc, p.scale, p.accumulate);
+    }
 }
 
 template <int MODE>
@@ -138,7 +142,8 @@ const void* ar_kernel_for(int K, int W) {
 
 }  // namespace
 
-cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaStream_t s) {
+cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaStream_t s,
+                                  int max_blocks) {
     const void* k;
     dim3 grid;
     if (width > 0) {
@@ -156,6 +161,10 @@ cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaSt
         cudaError_t e = blocks_per_chunk(k, p.K, uint64_t(p.S), &gx);
         if (e != cudaSuccess) return e;
         grid = dim3(gx, p.K);
+    }
+    if (max_blocks > 0) {
+        const unsigned cap = unsigned(max_blocks / p.K > 0 ? max_blocks / p.K : 1);
+        if (grid.x > cap) grid.x = cap;
     }
     void* args[] = {const_cast<RsParams*>(&p)};
     return cudaLaunchKernel(k, grid, dim3(kThreads), args, 0, s);

@@ -234,6 +234,63 @@ dpr_status dpr_allgather_coalesced(const dpr_coalesced_plan* plan, const void* c
 dpr_status dpr_coalesced_plan_destroy(dpr_coalesced_plan* plan);
 
 /*
+ * Stream-overlapped bucket pipeline.  The issue "ZeRO-1/2 average_tensor
+ * serializes backward compute behind the preceding reduction" (DeepSpeed
+ * issue 8364) states the ordering a ZeRO bucket reduction needs when
+ * gradients are gathered into a ring of physical IPG buffers on the compute
+ * stream and reduced on a separate reduction stream:
+ *   - the reduction of a bucket waits for every stream that produced its
+ *     gradients (multi-producer dependency);
+ *   - a physical buffer is not overwritten while the reduction of its
+ *     previous bucket still reads it (ping-pong reuse);
+ * and shows that making the compute stream wait for ALL queued reductions at
+ * every enqueue serialises compute behind the previous bucket's collective.
+ * Its proposed fix waits, per physical buffer, only for that buffer's last
+ * reduction.  Both behaviours are available for comparison:
+ *   DPR_WAIT_PER_BUFFER        the per-buffer completion events (the fix);
+ *   DPR_WAIT_REDUCTION_STREAM  the reverse wait on the whole reduction stream.
+ *
+ * dpr_bucket_pipeline_create allocates n_buffers (1..16) IPG buffers of K
+ * rank slices of bucket_capacity bf16 elements each (cudaMalloc), a
+ * non-blocking reduction stream and one completion event per buffer.
+ * max_blocks > 0 caps each reduction at about that many thread blocks, so the
+ * reduction leaves SMs to compute running beside it (as NCCL runs its
+ * collectives on a small grid); 0 lets a reduction use the whole GPU.
+ *
+ * dpr_bucket_pipeline_submit, for one bucket described by a flatten plan:
+ *   1. makes current_stream wait for each of the n_producers streams;
+ *   2. makes current_stream wait for the chosen buffer's previous reduction
+ *      (DPR_WAIT_PER_BUFFER) or for all queued reductions;
+ *   3. on current_stream, zeroes bucket positions no gradient covers and
+ *      gathers the bucket (dpr_flatten_bucket) into the next physical buffer;
+ *   4. on the reduction stream, after step 3, reduce-scatters the buffer into
+ *      out (as dpr_reduce_scatter with M = 1, mode, scale, accumulate) and
+ *      records the buffer's completion event.
+ * Requires plan K == the pipeline's K and bucket_numel <= bucket_capacity.
+ * out must stay valid until the reduction completes.
+ *
+ * dpr_bucket_pipeline_flush makes current_stream wait for every submitted
+ * reduction (the epilogue of a backward pass).  dpr_bucket_pipeline_stream
+ * returns the reduction stream (a cudaStream_t owned by the pipeline) so that
+ * callers can order other work against it.  dpr_bucket_pipeline_destroy
+ * waits for the reduction stream and frees everything.
+ */
+#define DPR_WAIT_PER_BUFFER 0
+#define DPR_WAIT_REDUCTION_STREAM 1
+
+typedef struct dpr_bucket_pipeline dpr_bucket_pipeline;
+
+dpr_status dpr_bucket_pipeline_create(dpr_bucket_pipeline** pipeline, int K, int64_t bucket_capacity,
+                                      int n_buffers, int wait_policy, int max_blocks);
+dpr_status dpr_bucket_pipeline_submit(dpr_bucket_pipeline* pipeline, const dpr_flatten_plan* plan,
+                                      float* const* out, int mode, float scale, int accumulate,
+                                      void* const* producers, int n_producers,
+                                      void* current_stream);
+dpr_status dpr_bucket_pipeline_flush(dpr_bucket_pipeline* pipeline, void* current_stream);
+dpr_status dpr_bucket_pipeline_stream(const dpr_bucket_pipeline* pipeline, void** stream);
+dpr_status dpr_bucket_pipeline_destroy(dpr_bucket_pipeline* pipeline);
+
+/*
  * Bucket formation, host only (DeepSpeed ZeRO-3 source walkthrough, sections
  * 3.1, 5.1, 5.4): gradients in arrival order are appended at the running
  * offset; the bucket is flushed first when adding the next gradient would

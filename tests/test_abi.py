@@ -35,7 +35,7 @@ def _declared():
 
 def test_exports_every_declared_function(L):
     names = _declared()
-    assert len(names) == 16
+    assert len(names) == 21
     for n in names:
         assert hasattr(L, n), n
 
@@ -178,3 +178,16 @@ def test_coalesced_rejections(L):
     assert L.dpr_reduce_scatter_coalesced(None, None, 0, 1.0, 0, None) == INVALID
     assert L.dpr_allgather_coalesced(None, None, None) == INVALID
     assert L.dpr_coalesced_plan_destroy(None) == OK
+
+
+def test_pipeline_rejections(L):
+    h = ctypes.c_void_p()
+    assert L.dpr_bucket_pipeline_create(ctypes.byref(h), 1, 1024, 2, 0, 0) == INVALID   # K < 2
+    assert L.dpr_bucket_pipeline_create(ctypes.byref(h), 4, 1024, 0, 0, 0) == INVALID   # no buffers
+    assert L.dpr_bucket_pipeline_create(ctypes.byref(h), 4, 1024, 2, 9, 0) == INVALID   # policy
+    assert L.dpr_bucket_pipeline_create(ctypes.byref(h), 4, 0, 2, 0, 0) == INVALID      # capacity
+    assert L.dpr_bucket_pipeline_create(ctypes.byref(h), 4, 1024, 2, 0, -1) == INVALID  # budget
+    assert h.value is None
+    assert L.dpr_bucket_pipeline_submit(None, None, None, 0, 1.0, 0, None, 0, None) == INVALID
+    assert L.dpr_bucket_pipeline_flush(None, None) == INVALID
+    assert L.dpr_bucket_pipeline_destroy(None) == OK
