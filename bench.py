@@ -50,6 +50,7 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 STEP_KERNELS = ("flatten", "rs_fp32_m2", "rs_hop_m2_acc", "allgather", "allreduce")
 Z3_KERNELS = ("rs_coalesced", "ag_coalesced")
+BF16_KERNELS = ("rs_bf16_copy", "rs_bf16_add", "cast")
 
 # DRAM traffic per launch from one ncu capture of each kernel (read + write
 # bytes, scaled to the bench's launch size), valid only while the kernel
@@ -76,12 +77,14 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
-    p.add_argument("--workload", choices=["zero_bucket", "zero3_per_param", "bucket_pipeline"],
+    p.add_argument("--workload", choices=["zero_bucket", "zero3_per_param", "bucket_pipeline",
+                                          "bf16_partition"],
                    default="zero_bucket",
                    help="zero_bucket: the headline step (default); zero3_per_param: the ZeRO-3 "
                         "discrete path on config 3's 56 gradients; bucket_pipeline: backward "
-                        "time under the stream-overlap policies")
-    p.add_argument("--only", choices=STEP_KERNELS + Z3_KERNELS, default=None,
+                        "time under the stream-overlap policies; bf16_partition: reduce-scatter "
+                        "into bf16 partitions over two micro steps and the step-time cast")
+    p.add_argument("--only", choices=STEP_KERNELS + Z3_KERNELS + BF16_KERNELS, default=None,
                    help="profile helper: launch only this kernel per step")
     p.add_argument("--n-per-rank", type=int, default=None,
                    help="profile helper: elements per rank (a multiple of 2**24) for a small "
@@ -348,6 +351,52 @@ class Zero3Workload:
         self.ag_plan.close()
 
 
+class Bf16PartitionWorkload:
+    """The ZeRO-3 literal partition data flow at K=8, 1 GiB per rank: micro
+    step 0 reduce-scatters into bf16 partition shards (copy_), micro step 1
+    reduce-scatters the next micro-batch and adds in bf16 (add_), and step()
+    casts the partition to fp32."""
+    kernels = ("rs_bf16_copy", "rs_bf16_add", "cast")
+
+    def __init__(self, dev, stream):
+        import torch
+        import gradient_reduction_gb300 as dpr
+        from workloads import configs as C
+        self.dpr, self.torch, self.dev, self.stream = dpr, torch, dev, stream
+        w = C.BENCH
+        K, N = w.K, w.N
+        S = N // K
+        with torch.cuda.stream(stream):
+            self.x = torch.empty(2, K, N, dtype=torch.bfloat16, device=dev)
+            for m, key in ((0, w.micro0_key), (1, lambda r: w.frag_key(r, 0))):
+                for r in range(K):
+                    w.dist.fill(0, N, key(r), device=dev, out=self.x[m, r])
+            self.part = torch.empty(K, S, dtype=torch.bfloat16, device=dev)
+            self.f32 = torch.empty(K * S, dtype=torch.float32, device=dev)
+        stream.synchronize()
+        self.K, self.N, self.S = K, N, S
+        self.bytes = {"rs_bf16_copy": 2 * K * N + 2 * N, "rs_bf16_add": 2 * K * N + 4 * N,
+                      "cast": 6 * N}
+
+    def launch(self, name):
+        dpr, K, N, s = self.dpr, self.K, self.N, self.stream
+        if name == "rs_bf16_copy":
+            dpr.dpr_reduce_scatter_bf16(list(self.x[0].unbind(0)), K, 1, N, list(self.part.unbind(0)),
+                                        stream=s)
+        elif name == "rs_bf16_add":
+            dpr.dpr_reduce_scatter_bf16(list(self.x[1].unbind(0)), K, 1, N, list(self.part.unbind(0)),
+                                        accumulate=True, stream=s)
+        elif name == "cast":
+            dpr.dpr_cast_bf16_to_fp32(self.part.view(-1), self.f32, stream=s)
+        else:
+            raise ValueError(name)
+
+    step = Workload.step
+
+    def close(self):
+        pass
+
+
 class PipelineBackward:
     """A simulated backward pass for the bucket pipeline: 16 buckets (one
     gradient per rank each, K=8, alternately 3 * 2**23 and 2**23 elements),
@@ -492,6 +541,9 @@ def run_device(args, rank, world, local_rank):
     if args.workload == "zero3_per_param":
         wl = Zero3Workload(dev, stream)
         kernels = (args.only,) if args.only else Z3_KERNELS
+    elif args.workload == "bf16_partition":
+        wl = Bf16PartitionWorkload(dev, stream)
+        kernels = (args.only,) if args.only else BF16_KERNELS
     else:
         wl = Workload(dev, stream, args.n_per_rank)
         kernels = (args.only,) if args.only else STEP_KERNELS
@@ -761,9 +813,17 @@ def main(argv=None):
                           "parallelism": "single GPU, 8 simulated ranks",
                           "l2": "inputs (42 GB resident) far larger than L2; no flush needed"}
         line["e2e"] = None
+    if args.workload == "bf16_partition":
+        line["config"] = {"workload": "zero3_bf16_partition_k8_1GiB", "K": 8,
+                          "elements_per_rank": res["wl"].N,
+                          "step": "RS into bf16 partitions (copy_) + RS with bf16 add_ + "
+                                  "step-time cast to fp32",
+                          "parallelism": "single GPU, 8 simulated ranks",
+                          "l2": "inputs (16 GiB resident) far larger than L2; no flush needed"}
+        line["e2e"] = None
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if args.workload == "zero3_per_param":
+    if args.workload in ("zero3_per_param", "bf16_partition"):
         res["wl"].close()
     else:
         res["wl"].plan.close()

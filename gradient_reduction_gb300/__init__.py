@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     dpr_allreduce,
     dpr_allgather_coalesced,
     dpr_bucket_assign,
+    dpr_cast_bf16_to_fp32,
     dpr_coalesced_plan_create,
     dpr_coalesced_plan_destroy,
     dpr_flatten_bucket,
@@ -27,6 +28,7 @@ from ._binding import (  # noqa: F401
     dpr_flatten_plan_create,
     dpr_flatten_plan_destroy,
     dpr_reduce_scatter,
+    dpr_reduce_scatter_bf16,
     dpr_reduce_scatter_coalesced,
     dpr_strerror,
     dpr_version,

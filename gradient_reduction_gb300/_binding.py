@@ -28,6 +28,9 @@ _SIGS = {
     "dpr_reduce_scatter": [_pp, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _pp, ctypes.c_int,
                            ctypes.c_float, ctypes.c_int, _c_p],
     "dpr_allgather": [_pp, ctypes.c_int, ctypes.c_int64, _pp, _c_p],
+    "dpr_reduce_scatter_bf16": [_pp, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _pp, ctypes.c_int,
+                                ctypes.c_float, ctypes.c_int, _c_p],
+    "dpr_cast_bf16_to_fp32": [_c_p, _c_p, ctypes.c_int64, _c_p],
     "dpr_allreduce": [_pp, ctypes.c_int, ctypes.c_int64, _pp, ctypes.c_int, ctypes.c_float, _c_p],
     "dpr_flatten_plan_create": [ctypes.POINTER(_c_p), ctypes.c_int, ctypes.c_int, _pp, _i64p,
                                 _i64p, ctypes.c_int64, _c_p],
@@ -124,6 +127,29 @@ def dpr_reduce_scatter(inputs: Sequence[torch.Tensor], K: int, M: int, N: int,
                                   1.0 / K if scale is None else scale, int(bool(accumulate)),
                                   _stream(stream))
     _check("dpr_reduce_scatter", st)
+
+
+def dpr_reduce_scatter_bf16(inputs: Sequence[torch.Tensor], K: int, M: int, N: int,
+                            outputs: Sequence[torch.Tensor], mode=RING_FP32,
+                            scale: float | None = None, accumulate: bool = False,
+                            stream=None) -> None:
+    """inputs[m*K + r]: bf16 (N,); outputs[j]: bf16 partition shard (N/K,)."""
+    if N > 0:
+        _need(inputs, M * K, torch.bfloat16, N, "inputs")
+        _need(outputs, K, torch.bfloat16, N // K if K else 0, "outputs")
+    st = lib().dpr_reduce_scatter_bf16(_ptrs(inputs), K, M, N, _ptrs(outputs), _MODES[mode],
+                                       1.0 / K if scale is None else scale, int(bool(accumulate)),
+                                       _stream(stream))
+    _check("dpr_reduce_scatter_bf16", st)
+
+
+def dpr_cast_bf16_to_fp32(inp: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """out[:n] = fp32(inp[:n]), n = inp.numel()."""
+    n = inp.numel()
+    _need([inp], 1, torch.bfloat16, n, "in")
+    _need([out], 1, torch.float32, n, "out")
+    _check("dpr_cast_bf16_to_fp32", lib().dpr_cast_bf16_to_fp32(inp.data_ptr(), out.data_ptr(), n,
+                                                                _stream(stream)))
 
 
 def dpr_allgather(shards: Sequence[torch.Tensor], K: int, N: int,

@@ -165,6 +165,63 @@ dpr_status dpr::reduce_scatter_capped(const void* const* in, int K, int M, int64
 
 extern "C" {
 
+dpr_status dpr_reduce_scatter_bf16(const void* const* in, int K, int M, int64_t N,
+                                   void* const* out, int mode, float scale, int accumulate,
+                                   void* stream) {
+    dpr_status st = check_kn(K, N);
+    if (st != DPR_OK) return st;
+    if (M < 1 || M > DPR_MAX_MICRO) return DPR_ERR_INVALID_ARG;
+    if (mode != DPR_SUM_RING_FP32 && mode != DPR_SUM_HOP_BF16) return DPR_ERR_INVALID_ARG;
+    if (N == 0) return DPR_OK;
+    if (!in || !out) return DPR_ERR_INVALID_ARG;
+    const int64_t S = N / K;
+    bool a16 = true, a32 = true;
+    std::vector<Span> outs;
+    for (int i = 0; i < M * K; ++i) {
+        if (!in[i]) return DPR_ERR_INVALID_ARG;
+        if (!aligned(in[i], 2)) return DPR_ERR_ALIGNMENT;
+        a16 = a16 && aligned(in[i], 16);
+        a32 = a32 && aligned(in[i], 32);
+    }
+    for (int j = 0; j < K; ++j) {
+        if (!out[j]) return DPR_ERR_INVALID_ARG;
+        if (!aligned(out[j], 2)) return DPR_ERR_ALIGNMENT;
+        a16 = a16 && aligned(out[j], 16);
+        a32 = a32 && aligned(out[j], 32);
+        outs.push_back(span_of(out[j], uint64_t(S) * 2));
+    }
+    if (!pairwise_disjoint(outs)) return DPR_ERR_ALIAS;
+    for (int i = 0; i < M * K; ++i) {
+        const Span a = span_of(in[i], uint64_t(N) * 2);
+        for (const Span& o : outs)
+            if (overlaps(a, o)) return DPR_ERR_ALIAS;
+    }
+    const int width = access_width(S, a32, a16);
+    RsParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int i = 0; i < M * K; ++i) p.in[i] = static_cast<const uint16_t*>(in[i]);
+    for (int j = 0; j < K; ++j) p.out[j] = static_cast<float*>(out[j]);
+    p.S = S;
+    p.su = width > 0 ? uint32_t(S / (2 * width)) : 0;
+    p.K = K;
+    p.M = M;
+    p.scale = scale;
+    p.accumulate = accumulate ? 1 : 0;
+    return cuda_status(launch_reduce_scatter_bf16(p, mode, width, static_cast<cudaStream_t>(stream)));
+}
+
+dpr_status dpr_cast_bf16_to_fp32(const void* in, float* out, int64_t n, void* stream) {
+    if (n < 0) return DPR_ERR_INVALID_ARG;
+    if (n > DPR_MAX_ELEMS * DPR_MAX_RANKS) return DPR_ERR_UNSUPPORTED;
+    if (n == 0) return DPR_OK;
+    if (!in || !out) return DPR_ERR_INVALID_ARG;
+    if (!aligned(in, 2) || !aligned(out, 4)) return DPR_ERR_ALIGNMENT;
+    if (overlaps(span_of(in, uint64_t(n) * 2), span_of(out, uint64_t(n) * 4))) return DPR_ERR_ALIAS;
+    const bool vec = aligned(in, 32) && aligned(out, 32);
+    return cuda_status(launch_cast(static_cast<const uint16_t*>(in), out, uint64_t(n), vec,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
 dpr_status dpr_allgather(const void* const* shard, int K, int64_t N, void* const* out,
                          void* stream) {
     dpr_status st = check_kn(K, N);

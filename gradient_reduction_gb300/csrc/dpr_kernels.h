@@ -86,6 +86,9 @@ dpr_status reduce_scatter_capped(const void* const* in, int K, int M, int64_t N,
                                  int mode, float scale, int accumulate, cudaStream_t stream,
                                  int max_blocks);
 cudaError_t launch_allreduce(const ArParams& p, int mode, int width, cudaStream_t s);
+// bf16 partition shards (RsParams::out points at bf16 buffers).
+cudaError_t launch_reduce_scatter_bf16(const RsParams& p, int mode, int width, cudaStream_t s);
+cudaError_t launch_cast(const uint16_t* in, float* out, uint64_t n, bool vec, cudaStream_t s);
 cudaError_t launch_allgather(const AgParams& p, int width, cudaStream_t s);
 cudaError_t launch_flatten(const FlatParams& p, cudaStream_t s);
 

@@ -41,6 +41,88 @@ __global__ void __launch_bounds__(kThreads) rs_vec(const __grid_constant__ RsPar
     }
 }
 
+// bf16 partition shards (the ZeRO-3 partition buffer): the shard is rounded
+// once to bf16, bf16(fp32(acc) * scale); with accumulate it is added in bf16
+// to the existing shard, bf16(old + shard) (copy_ / add_ of the walkthrough's
+// section 5.3).  RsParams::out holds bf16 buffers here.
+template <int W>
+__device__ __forceinline__ void store_shard_bf16(uint16_t* o, const float (&acc)[2 * W], float scale,
+                                                 int accumulate) {
+    uint32_t w[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+        w[k] = pack_bf16x2(__fmul_rn(acc[2 * k], scale), __fmul_rn(acc[2 * k + 1], scale));
+    if (accumulate) {
+        uint32_t old[W];
+        load_words<W, false>(o, old);
+#pragma unroll
+        for (int k = 0; k < W; ++k) w[k] = add_bf16x2(old[k], w[k]);
+    }
+    store_words<W>(o, w);
+}
+
+template <int KC, int M, int MODE, int W>
+__global__ void __launch_bounds__(kThreads) rs_bf16_vec(const __grid_constant__ RsParams p) {
+    const int j = blockIdx.y;
+    uint16_t* const out = reinterpret_cast<uint16_t*>(p.out[j]);
+    for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < p.su;
+         t += uint64_t(gridDim.x) * kThreads) {
+        const uint64_t e = uint64_t(j) * uint64_t(p.S) + uint64_t(2 * W) * t;
+        float acc[2 * W];
+        ring_sum<KC, M, MODE, W, true>(p.in, p.K, j, e, acc);
+        store_shard_bf16<W>(out + uint64_t(2 * W) * t, acc, p.scale, p.accumulate);
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads) rs_bf16_scalar(const __grid_constant__ RsParams p) {
+    const int j = blockIdx.y, K = p.K, M = p.M;
+    const uint64_t S = uint64_t(p.S), base = uint64_t(j) * S;
+    uint16_t* const out = reinterpret_cast<uint16_t*>(p.out[j]);
+    for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < S;
+         t += uint64_t(gridDim.x) * kThreads) {
+        const uint64_t e = base + t;
+        float acc = 0.0f;
+        uint16_t hop = 0;
+        for (int s = 0; s < K; ++s) {
+            int r = j + s;
+            r = (r >= K) ? r - K : r;
+            uint16_t x = p.in[r][e];
+            if (M == 2) x = add_bf16(x, p.in[K + r][e]);
+            if constexpr (MODE == DPR_SUM_RING_FP32) acc = (s == 0) ? bf_1(x) : __fadd_rn(acc, bf_1(x));
+            else hop = (s == 0) ? x : add_bf16(hop, x);
+        }
+        if constexpr (MODE == DPR_SUM_HOP_BF16) acc = bf_1(hop);
+        uint16_t v = to_bf16(__fmul_rn(acc, p.scale));
+        if (p.accumulate) v = add_bf16(out[t], v);
+        out[t] = v;
+    }
+}
+
+// step()-time cast of a bf16 partition to fp32 (exact widening); one unit of
+// 16 elements per thread, 32-byte loads and stores when both buffers allow.
+__global__ void __launch_bounds__(kThreads) cast_bf16_fp32(const uint16_t* __restrict__ in,
+                                                           float* __restrict__ out, uint64_t n,
+                                                           int vec) {
+    const uint64_t u = uint64_t(blockIdx.x) * kThreads + threadIdx.x;
+    const uint64_t e0 = 16 * u;
+    if (e0 >= n) return;
+    if (vec && e0 + 16 <= n) {
+        uint32_t w[8];
+        load_words<8, true>(in + e0, w);
+        float f[16];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            f[2 * k] = bf_lo(w[k]);
+            f[2 * k + 1] = bf_hi(w[k]);
+        }
+        st_f8(out + e0, f);
+        st_f8(out + e0 + 8, f + 8);
+        return;
+    }
+    for (uint64_t e = e0; e < n && e < e0 + 16; ++e) out[e] = bf_1(in[e]);
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads) rs_scalar(const __grid_constant__ RsParams p) {
     const int j = blockIdx.y, K = p.K, M = p.M;
@@ -126,6 +208,13 @@ const void* rs_kernel_for(int K, int W) {
     }
 }
 
+template <int M, int MODE>
+const void* rs_bf16_kernel_for(int K, int W) {
+    if (W == 4) return reinterpret_cast<const void*>(rs_bf16_vec<0, M, MODE, 4>);
+    if (K == 8) return reinterpret_cast<const void*>(rs_bf16_vec<8, M, MODE, 8>);
+    return reinterpret_cast<const void*>(rs_bf16_vec<0, M, MODE, 8>);
+}
+
 template <int MODE>
 const void* ar_kernel_for(int K, int W) {
     if (W == 4) return reinterpret_cast<const void*>(ar_vec<0, MODE, 4>);
@@ -168,6 +257,39 @@ cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaSt
     }
     void* args[] = {const_cast<RsParams*>(&p)};
     return cudaLaunchKernel(k, grid, dim3(kThreads), args, 0, s);
+}
+
+cudaError_t launch_reduce_scatter_bf16(const RsParams& p, int mode, int width, cudaStream_t s) {
+    const void* k;
+    dim3 grid;
+    if (width > 0) {
+        if (mode == DPR_SUM_RING_FP32)
+            k = (p.M == 1) ? rs_bf16_kernel_for<1, DPR_SUM_RING_FP32>(p.K, width)
+                           : rs_bf16_kernel_for<2, DPR_SUM_RING_FP32>(p.K, width);
+        else
+            k = (p.M == 1) ? rs_bf16_kernel_for<1, DPR_SUM_HOP_BF16>(p.K, width)
+                           : rs_bf16_kernel_for<2, DPR_SUM_HOP_BF16>(p.K, width);
+        grid = dim3(unsigned((uint64_t(p.su) + kThreads - 1) / kThreads), p.K);
+    } else {
+        k = (mode == DPR_SUM_RING_FP32)
+                ? reinterpret_cast<const void*>(rs_bf16_scalar<DPR_SUM_RING_FP32>)
+                : reinterpret_cast<const void*>(rs_bf16_scalar<DPR_SUM_HOP_BF16>);
+        int gx = 1;
+        cudaError_t e = blocks_per_chunk(k, p.K, uint64_t(p.S), &gx);
+        if (e != cudaSuccess) return e;
+        grid = dim3(gx, p.K);
+    }
+    void* args[] = {const_cast<RsParams*>(&p)};
+    return cudaLaunchKernel(k, grid, dim3(kThreads), args, 0, s);
+}
+
+cudaError_t launch_cast(const uint16_t* in, float* out, uint64_t n, bool vec, cudaStream_t s) {
+    const uint64_t units = (n + 15) / 16;
+    const unsigned blocks = unsigned((units + kThreads - 1) / kThreads);
+    int v = vec ? 1 : 0;
+    void* args[] = {&in, &out, &n, &v};
+    return cudaLaunchKernel(reinterpret_cast<const void*>(cast_bf16_fp32), dim3(blocks),
+                            dim3(kThreads), args, 0, s);
 }
 
 cudaError_t launch_allreduce(const ArParams& p, int mode, int width, cudaStream_t s) {

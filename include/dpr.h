@@ -86,6 +86,28 @@ dpr_status dpr_reduce_scatter(const void* const* in, int K, int M, int64_t N,
                               void* stream);
 
 /*
+ * Reduce-scatter into bf16 partition shards: the literal ZeRO-3 data flow
+ * (DeepSpeed ZeRO-3 source walkthrough, sections 1, 5.3 and 8), where the
+ * reduced shard lands in the rank's bf16 partition buffer -- copy_ on the
+ * first micro step, add_ (in bf16) on later ones -- and the one bf16 -> fp32
+ * conversion happens later, in step() (dpr_cast_bf16_to_fp32).
+ *     accumulate == 0:  out[j][t] = bf16(fp32(acc) * scale)
+ *     accumulate != 0:  out[j][t] = bf16(out[j][t] + bf16(fp32(acc) * scale))
+ * acc, in, K, M, N, mode and scale exactly as dpr_reduce_scatter; out: host
+ * array [K] of bf16 shards of N/K elements, not overlapping each other or any
+ * input.
+ */
+dpr_status dpr_reduce_scatter_bf16(const void* const* in, int K, int M, int64_t N,
+                                   void* const* out, int mode, float scale, int accumulate,
+                                   void* stream);
+
+/*
+ * The step()-time cast of a bf16 partition to fp32 (exact widening):
+ * out[t] = fp32(in[t]), n elements; in and out must not overlap.
+ */
+dpr_status dpr_cast_bf16_to_fp32(const void* in, float* out, int64_t n, void* stream);
+
+/*
  * Ring all-gather of K shards into K full replicas.
  *
  * Defines: lecture section 3.2 and CSDN Phase 2 (complete chunks travel the

@@ -282,3 +282,31 @@ def allgather_coalesced(partitions: list, numel: list, K: int) -> list:
         for r in range(K):
             params[r][p] = outs[r][:n].copy()
     return params
+
+
+# ---- bf16 partition buffer and the step-time cast (ZeRO-3 literal data flow) --------
+#
+# DeepSpeed ZeRO-3 source walkthrough, section 5.3: the reduced shard is copied
+# into the rank's bf16 partition buffer on the first micro step and added to it
+# (add_, in bf16) on later ones; sections 1 and 8: the only bf16 -> fp32
+# conversion happens in step().  Reading: the collective's shard is rounded to
+# bf16 once, bf16(fp32(sum) * scale); add_ rounds the fp32 sum of the two bf16
+# values once more to bf16.
+
+def reduce_scatter_bf16(x: list, K: int, M: int = 1, mode: int = RING_FP32,
+                        scale: float = 1.0, out_init: list | None = None):
+    """As reduce_scatter, with bf16 partition shards (uint16 bits).
+    out_init: None (copy) or K uint16 arrays of N/K to add into."""
+    shards, ctr = reduce_scatter(x, K, M, mode, scale)
+    out = []
+    for j in range(K):
+        s = bf16.from_f32(shards[j])
+        if out_init is not None:
+            s = bf16.add(np.asarray(out_init[j], dtype=np.uint16), s)
+        out.append(s)
+    return out, ctr
+
+
+def cast_partition(bits: np.ndarray) -> np.ndarray:
+    """step()-time cast of a bf16 partition to fp32 (exact widening)."""
+    return bf16.to_f32(bits).copy()

@@ -30,12 +30,12 @@ def L():
 def _declared():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(dpr_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(dpr_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_exports_every_declared_function(L):
     names = _declared()
-    assert len(names) == 21
+    assert len(names) == 23
     for n in names:
         assert hasattr(L, n), n
 
@@ -191,3 +191,17 @@ def test_pipeline_rejections(L):
     assert L.dpr_bucket_pipeline_submit(None, None, None, 0, 1.0, 0, None, 0, None) == INVALID
     assert L.dpr_bucket_pipeline_flush(None, None) == INVALID
     assert L.dpr_bucket_pipeline_destroy(None) == OK
+
+
+def test_bf16_partition_rejections(L):
+    K, N = 4, 64
+    ins, outs = _bufs(K, 1 << 20), _bufs(K, 1 << 20, BASE + (1 << 30))
+    rs = L.dpr_reduce_scatter_bf16
+    assert rs(_arr(ins), K, 1, N + 1, _arr(outs), 0, 1.0, 0, None) == INVALID
+    assert rs(_arr(ins), K, 1, N, _arr(outs[:3] + [outs[3] + 1]), 0, 1.0, 0, None) == ALIGN
+    assert rs(_arr(ins), K, 1, N, _arr(outs[:3] + [ins[0]]), 0, 1.0, 0, None) == ALIAS
+    c = L.dpr_cast_bf16_to_fp32
+    assert c(ctypes.c_void_p(BASE), ctypes.c_void_p(BASE + 2), 16, None) == ALIGN
+    assert c(ctypes.c_void_p(BASE), ctypes.c_void_p(BASE + 16), 16, None) == ALIAS
+    assert c(None, None, 0, None) == OK
+    assert c(ctypes.c_void_p(BASE), ctypes.c_void_p(BASE + 4096), -1, None) == INVALID
