@@ -21,6 +21,11 @@ from ._binding import (  # noqa: F401
     dpr_allgather_coalesced,
     dpr_bucket_assign,
     dpr_cast_bf16_to_fp32,
+    dpr_cost_allreduce,
+    dpr_cost_best_segments,
+    dpr_cost_crossover,
+    dpr_cost_dp_speedup,
+    dpr_cost_ring_broadcast,
     dpr_coalesced_plan_create,
     dpr_coalesced_plan_destroy,
     dpr_flatten_bucket,

@@ -54,6 +54,17 @@ _SIGS = {
     "dpr_bucket_pipeline_flush": [_c_p, _c_p],
     "dpr_bucket_pipeline_stream": [_c_p, ctypes.POINTER(_c_p)],
     "dpr_bucket_pipeline_destroy": [_c_p],
+    "dpr_cost_allreduce": [ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                           ctypes.c_double, ctypes.POINTER(ctypes.c_double)],
+    "dpr_cost_ring_broadcast": [ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                ctypes.c_int64, ctypes.POINTER(ctypes.c_double)],
+    "dpr_cost_best_segments": [ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                               ctypes.c_int64, ctypes.POINTER(ctypes.c_int64),
+                               ctypes.POINTER(ctypes.c_double)],
+    "dpr_cost_crossover": [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                           ctypes.c_double, ctypes.POINTER(ctypes.c_double)],
+    "dpr_cost_dp_speedup": [ctypes.c_double, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                            ctypes.c_double, ctypes.POINTER(ctypes.c_double)],
     "dpr_strerror": [ctypes.c_int],
     "dpr_last_cuda_error": [],
     "dpr_version": [],
@@ -414,3 +425,44 @@ def dpr_strerror(status: int) -> str:
 
 def dpr_version() -> str:
     return lib().dpr_version().decode()
+
+
+ALGO_RING, ALGO_TREE, ALGO_NAIVE = 0, 1, 2
+_ALGOS = {"ring": ALGO_RING, "tree": ALGO_TREE, "naive": ALGO_NAIVE,
+          ALGO_RING: ALGO_RING, ALGO_TREE: ALGO_TREE, ALGO_NAIVE: ALGO_NAIVE}
+
+
+def dpr_cost_allreduce(algo, K: int, nbytes: float, alpha: float, beta: float) -> float:
+    out = ctypes.c_double()
+    _check("dpr_cost_allreduce", lib().dpr_cost_allreduce(_ALGOS[algo], K, nbytes, alpha, beta,
+                                                          ctypes.byref(out)))
+    return out.value
+
+
+def dpr_cost_ring_broadcast(K: int, nbytes: float, alpha: float, beta: float, segments: int = 1) -> float:
+    out = ctypes.c_double()
+    _check("dpr_cost_ring_broadcast", lib().dpr_cost_ring_broadcast(K, nbytes, alpha, beta, segments,
+                                                                    ctypes.byref(out)))
+    return out.value
+
+
+def dpr_cost_best_segments(K: int, nbytes: float, alpha: float, beta: float,
+                           max_segments: int = 1 << 20):
+    s, t = ctypes.c_int64(), ctypes.c_double()
+    _check("dpr_cost_best_segments", lib().dpr_cost_best_segments(K, nbytes, alpha, beta, max_segments,
+                                                                  ctypes.byref(s), ctypes.byref(t)))
+    return s.value, t.value
+
+
+def dpr_cost_crossover(algo_a, algo_b, K: int, alpha: float, beta: float) -> float:
+    out = ctypes.c_double()
+    _check("dpr_cost_crossover", lib().dpr_cost_crossover(_ALGOS[algo_a], _ALGOS[algo_b], K, alpha,
+                                                          beta, ctypes.byref(out)))
+    return out.value
+
+
+def dpr_cost_dp_speedup(t1: float, K: int, nbytes: float, alpha: float, beta: float) -> float:
+    out = ctypes.c_double()
+    _check("dpr_cost_dp_speedup", lib().dpr_cost_dp_speedup(t1, K, nbytes, alpha, beta,
+                                                            ctypes.byref(out)))
+    return out.value

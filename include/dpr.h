@@ -329,6 +329,38 @@ dpr_status dpr_bucket_assign(const int64_t* numel, int P, int64_t cap, int64_t p
                              int32_t* bucket_of, int64_t* offset, int64_t* bucket_numel,
                              int* n_buckets);
 
+/*
+ * Alpha-beta cost model (host only; CMU 11-868 Lecture 14 notes, sections 3.1,
+ * 3.4 and 4.4).  A message of n bytes costs alpha + n / beta seconds; K
+ * devices, `bytes` per device:
+ *   DPR_ALGO_RING   2(K-1) (alpha + bytes / (K beta))
+ *   DPR_ALGO_TREE   2 ceil(log2 K) (alpha + bytes / beta)
+ *   DPR_ALGO_NAIVE  2 (alpha + (K-1) bytes / beta)
+ * dpr_cost_ring_broadcast: a ring broadcast cut into S segments,
+ *   (K - 2 + S) (alpha + bytes / (S beta)); S = 1 is the unsegmented case.
+ * dpr_cost_best_segments: the best S among 1, 2, 4, ... <= max_segments.
+ * dpr_cost_crossover: the message size at which two all-reduce algorithms
+ *   cost the same (DPR_ERR_UNSUPPORTED if they never cross).
+ * dpr_cost_dp_speedup: T1 / (T1 / K + ring all-reduce time), the speed-up of
+ *   K-way data parallelism without overlap for a single-device step of T1.
+ * Invalid arguments (beta <= 0, negative sizes, unknown algorithm) return
+ * DPR_ERR_INVALID_ARG.
+ */
+#define DPR_ALGO_RING 0
+#define DPR_ALGO_TREE 1
+#define DPR_ALGO_NAIVE 2
+
+dpr_status dpr_cost_allreduce(int algo, int K, double bytes, double alpha, double beta,
+                              double* seconds);
+dpr_status dpr_cost_ring_broadcast(int K, double bytes, double alpha, double beta, int64_t segments,
+                                   double* seconds);
+dpr_status dpr_cost_best_segments(int K, double bytes, double alpha, double beta,
+                                  int64_t max_segments, int64_t* segments, double* seconds);
+dpr_status dpr_cost_crossover(int algo_a, int algo_b, int K, double alpha, double beta,
+                              double* bytes);
+dpr_status dpr_cost_dp_speedup(double t1, int K, double bytes, double alpha, double beta,
+                               double* speedup);
+
 /* Static description of a status code. */
 const char* dpr_strerror(int status);
 

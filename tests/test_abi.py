@@ -35,7 +35,7 @@ def _declared():
 
 def test_exports_every_declared_function(L):
     names = _declared()
-    assert len(names) == 23
+    assert len(names) == 28
     for n in names:
         assert hasattr(L, n), n
 
