@@ -53,16 +53,17 @@ Z3_KERNELS = ("rs_coalesced", "ag_coalesced")
 BF16_KERNELS = ("rs_bf16_copy", "rs_bf16_add", "cast")
 
 # DRAM traffic per launch from one ncu capture of each kernel (read + write
-# bytes, scaled to the bench's launch size), valid only while the kernel
-# sources hash to `src_sha`; otherwise reported as null.
+# bytes at the bench's launch size), valid only while the kernel's sources
+# hash to `src_sha`; otherwise reported as null.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum at the bench's full size
-    # (K=8, N=2**29), one launch each (profiles/step_k8_1GiB_dram_traffic.md)
-    "flatten": {"bytes": 17_128_000_000, "src_sha": "f9e4c54467eb0af7"},
-    "rs_fp32_m2": {"bytes": 19_312_000_000, "src_sha": "f9e4c54467eb0af7"},
-    "rs_hop_m2_acc": {"bytes": 21_461_000_000, "src_sha": "f9e4c54467eb0af7"},
-    "allgather": {"bytes": 9_601_000_000, "src_sha": "f9e4c54467eb0af7"},
-    "allreduce": {"bytes": 17_121_000_000, "src_sha": "f9e4c54467eb0af7"},
+    # (K=8, N=2**29), one launch each (profiles/step_k8_1GiB_dram_traffic.md); src_sha is
+    # kernel_src_sha(kernel) of the sources the capture was taken from
+    "flatten": {"bytes": 17_128_000_000, "src_sha": "81b7d453ae3c43eb"},
+    "rs_fp32_m2": {"bytes": 19_314_000_000, "src_sha": "7e627fc3de0cef69"},
+    "rs_hop_m2_acc": {"bytes": 21_460_000_000, "src_sha": "7e627fc3de0cef69"},
+    "allgather": {"bytes": 9_601_000_000, "src_sha": "81b7d453ae3c43eb"},
+    "allreduce": {"bytes": 17_123_000_000, "src_sha": "7e627fc3de0cef69"},
 }
 
 
@@ -78,7 +79,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--workload", choices=["zero_bucket", "zero3_per_param", "bucket_pipeline",
-                                          "bf16_partition"],
+                                          "bf16_partition", "sweep"],
                    default="zero_bucket",
                    help="zero_bucket: the headline step (default); zero3_per_param: the ZeRO-3 "
                         "discrete path on config 3's 56 gradients; bucket_pipeline: backward "
@@ -86,6 +87,8 @@ def parse_args(argv=None):
                         "into bf16 partitions over two micro steps and the step-time cast")
     p.add_argument("--only", choices=STEP_KERNELS + Z3_KERNELS + BF16_KERNELS, default=None,
                    help="profile helper: launch only this kernel per step")
+    p.add_argument("--graph", action="store_true",
+                   help="capture one step's launches in a CUDA graph and replay it")
     p.add_argument("--n-per-rank", type=int, default=None,
                    help="profile helper: elements per rank (a multiple of 2**24) for a small "
                         "case; the bench line is quoted only at the default 2**29")
@@ -136,10 +139,24 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_src_sha() -> str:
+# Source files that determine each timed kernel and its launch (kernel code,
+# shared device headers, host-side layout selection and grid sizing).
+_COMMON_SRC = ["dpr_device.cuh", "dpr_kernels.h", "dpr_api.cu"]
+KERNEL_SOURCES = {
+    "flatten": ["gather_kernels.cu"] + _COMMON_SRC,
+    "allgather": ["gather_kernels.cu"] + _COMMON_SRC,
+    "rs_fp32_m2": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
+    "rs_hop_m2_acc": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
+    "allreduce": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
+}
+
+
+def kernel_src_sha(kernel: str | None = None) -> str:
+    """Hash of the sources of one timed kernel (all of csrc/ when None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gradient_reduction_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = KERNEL_SOURCES.get(kernel) if kernel else None
+    for f in sorted(files or os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -488,6 +505,90 @@ class PipelineBackward:
             p.close()
 
 
+def run_sweep_bench(args):
+    """Configuration 5's sweep: effective GB/s of the reduce-scatter (both
+    modes, 2 micro-batches), all-gather and all-reduce for K in
+    {2,4,8,16,64} and 1 KiB .. 1 GiB per rank.  Each figure is algorithmic
+    bytes over the average launch time (CUDA events); small sizes show the
+    launch-bound regime."""
+    import torch
+    import gradient_reduction_gb300 as dpr
+    from workloads import configs as C
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = torch.cuda.Stream(device=dev)
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)     # > L2 (129 MB)
+
+    def timed(fn, working_set):
+        """Average launch time.  Working sets below 1 GiB are timed launch by
+        launch with the L2 flushed (a 512 MiB write) before each launch, so
+        no point is measured L2-resident."""
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            fn()
+        s.synchronize()
+        if working_set >= (1 << 30):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(args.steps):
+                fn()
+            b.record(s)
+            s.synchronize()
+            return a.elapsed_time(b) / 1e3 / args.steps
+        ts = []
+        for _ in range(args.steps):
+            with torch.cuda.stream(s):
+                flush.fill_(1)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            ts.append((a, b))
+        s.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ts) / 1e3 / len(ts)
+
+    table = []
+    for K, nbytes in C.cfg5_points():
+        N = nbytes // 2
+        S = N // K
+        row = {"K": K, "bytes_per_rank": nbytes}
+        x = torch.empty(2 * K, N, dtype=torch.bfloat16, device=dev).normal_()
+        xs = list(x.unbind(0))
+        out = torch.empty(K, S, dtype=torch.float32, device=dev)
+        outs = list(out.unbind(0))
+        for mode, name in ((dpr.RING_FP32, "rs_fp32_m2"), (dpr.HOP_BF16, "rs_hop_m2")):
+            t = timed(lambda: dpr.dpr_reduce_scatter(xs, K, 2, N, outs, mode=mode, stream=s),
+                      4 * K * N + 4 * N)
+            row[name] = round((4 * K * N + 4 * N) / t / 1e9, 1)
+        del xs, x, out, outs
+        torch.cuda.empty_cache()
+        x = torch.empty(K, N, dtype=torch.bfloat16, device=dev).normal_()
+        y = torch.empty(K, N, dtype=torch.bfloat16, device=dev)
+        xs, ys = list(x.unbind(0)), list(y.unbind(0))
+        t = timed(lambda: dpr.dpr_allreduce(xs, K, N, ys, stream=s), 4 * K * N)
+        row["allreduce"] = round(4 * K * N / t / 1e9, 1)
+        shards = [xs[j][:S] for j in range(K)]
+        t = timed(lambda: dpr.dpr_allgather(shards, K, N, ys, stream=s), 2 * N + 2 * K * N)
+        row["allgather"] = round((2 * N + 2 * K * N) / t / 1e9, 1)
+        del xs, ys, x, y, shards
+        torch.cuda.empty_cache()
+        table.append(row)
+        print(json.dumps(row), file=sys.stderr, flush=True)
+    peak, kind = load_peaks()
+    head = [r for r in table if r["K"] == 8 and r["bytes_per_rank"] == 1 << 30][0]
+    line = {"metric": METRIC, "value": head["rs_fp32_m2"], "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "config": {"workload": "cfg5_sweep", "K": [2, 4, 8, 16, 64],
+                       "bytes_per_rank": "1 KiB .. 1 GiB by 4x", "micro_batches": 2},
+            "value_is": "reduce-scatter ring fp32 M=2 at K=8, 1 GiB per rank",
+            "peak": peak, "peak_kind": kind, "table": table}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_pipeline_bench(args):
     import torch
     dev = torch.device("cuda", 0)
@@ -551,6 +652,14 @@ def run_device(args, rank, world, local_rank):
     for _ in range(args.warmup):
         wl.step(kernels)
     stream.synchronize()
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            wl.step(kernels)
+        for _ in range(args.warmup):
+            graph.replay()
+        stream.synchronize()
     barrier(dev)
     torch.cuda.synchronize()
     clocks = ClockSampler(local_rank).start() if rank == 0 else None
@@ -559,7 +668,11 @@ def run_device(args, rank, world, local_rank):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        wl.step(kernels, events)
+        if graph is not None:
+            with torch.cuda.stream(stream):
+                graph.replay()
+        else:
+            wl.step(kernels, events)
     t1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
@@ -567,6 +680,13 @@ def run_device(args, rank, world, local_rank):
     clk = clocks.stop() if clocks else None
     elapsed = t0.elapsed_time(t1) / 1e3
     max_elapsed = max_over_ranks(elapsed, dev)
+    launches = len(events)
+    if graph is not None:
+        # per-kernel times come from a short eager pass after the timed region
+        launches = args.steps * len(kernels)
+        for _ in range(min(args.steps, 20)):
+            wl.step(kernels, events)
+        stream.synchronize()
     per = {}
     for name, a, b in events:
         per.setdefault(name, []).append(a.elapsed_time(b) / 1e3)
@@ -581,7 +701,7 @@ def run_device(args, rank, world, local_rank):
         e2e = run_e2e(wl, args, step_bytes)
     return {"elapsed": elapsed, "max_elapsed": max_elapsed, "step_bytes": step_bytes,
             "kernels": kernels_out, "clocks": clk, "e2e": e2e, "wl": wl,
-            "launches": len(events)}
+            "launches": launches}
 
 
 def run_e2e(wl, args, step_bytes):
@@ -764,6 +884,8 @@ def main(argv=None):
         return run_reference(args)
     if args.workload == "bucket_pipeline":
         return run_pipeline_bench(args)
+    if args.workload == "sweep":
+        return run_sweep_bench(args)
     import torch
     rank, world, local_rank = dist_env()
     if world > 1:
@@ -776,7 +898,7 @@ def main(argv=None):
     d = kern[dom]
     sha = kernel_src_sha()
     tr = NCU_TRAFFIC.get(dom)
-    traffic = tr["bytes"] if tr and tr.get("src_sha") == sha else None
+    traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_sha(dom) else None
     value = job_value(res["step_bytes"], args.steps, world, res["max_elapsed"])
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -799,6 +921,8 @@ def main(argv=None):
     }
     if args.only:
         line["only"] = args.only
+    if args.graph:
+        line["graph"] = "one step captured in a CUDA graph and replayed; per-kernel figures from eager launches"
     if args.n_per_rank:
         line["config"]["elements_per_rank"] = wl_n = res["wl"].N
         line["config"]["bytes_per_rank"] = 2 * wl_n
