@@ -518,12 +518,14 @@ def run_sweep_bench(args):
     torch.cuda.set_device(dev)
     s = torch.cuda.Stream(device=dev)
 
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)     # > L2 (129 MB)
+    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)      # 512 MiB > L2 (129 MB)
 
     def timed(fn, working_set):
         """Average launch time.  Working sets below 1 GiB are timed launch by
-        launch with the L2 flushed (a 512 MiB write) before each launch, so
-        no point is measured L2-resident."""
+        launch with the L2 flushed before each launch by reading 512 MiB, so no
+        point is measured L2-resident (a read leaves clean lines; a write-based
+        flush would leave ~129 MB of dirty lines whose write-back the timed
+        kernel would pay for)."""
         torch.cuda.synchronize()
         for _ in range(args.warmup):
             fn()
@@ -540,7 +542,7 @@ def run_sweep_bench(args):
         ts = []
         for _ in range(args.steps):
             with torch.cuda.stream(s):
-                flush.fill_(1)
+                flush.sum()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(s)
@@ -717,7 +719,10 @@ def run_e2e(wl, args, step_bytes):
     step still moves all of its own bytes inside the timed region."""
     import torch
     dev = wl.dev
-    sets = [wl, Workload(dev, wl.stream, args.n_per_rank, fill=False)]
+    # two buffer sets (a third one measured no faster on GB300: the host link,
+    # not the set reuse, bounds the step)
+    nsets = 2
+    sets = [wl] + [Workload(dev, wl.stream, args.n_per_rank, fill=False) for _ in range(nsets - 1)]
     h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl.inputs()]
     h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl.outputs()]
     for h, d in zip(h_in, wl.inputs()):
@@ -729,13 +734,13 @@ def run_e2e(wl, args, step_bytes):
     for w in sets:
         w.stream = s_comp
     n = args.e2e_steps
-    in_done = [torch.cuda.Event() for _ in range(2)]
-    comp_done = [None, None]
-    out_done = [None, None]
+    in_done = [torch.cuda.Event() for _ in range(nsets)]
+    comp_done = [None] * nsets
+    out_done = [None] * nsets
 
     def run(steps):
         for i in range(steps):
-            b = i % 2
+            b = i % nsets
             w = sets[b]
             # copies in: wait until step i-2 has finished with this set
             if comp_done[b] is not None:
@@ -759,7 +764,7 @@ def run_e2e(wl, args, step_bytes):
             ev2.record(s_out)
             out_done[b] = ev2
 
-    run(2)                                   # warm-up of both buffer sets
+    run(nsets)                               # warm-up of every buffer set
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -767,13 +772,14 @@ def run_e2e(wl, args, step_bytes):
     s_comp.wait_event(t0)
     s_out.wait_event(t0)
     run(n)
-    s_in.wait_event(out_done[(n - 1) % 2])
+    s_in.wait_event(out_done[(n - 1) % nsets])
     t1.record(s_in)
     torch.cuda.synchronize()
     el = t0.elapsed_time(t1) / 1e3
     el = max_over_ranks(el, dev)
     _, world, _ = dist_env()
-    sets[1].plan.close()
+    for w in sets[1:]:
+        w.plan.close()
     for w in sets:
         w.stream = wl.stream
     return {"value": round(job_value(step_bytes, n, world, el), 1), "unit": UNIT,
