@@ -221,6 +221,12 @@ dpr_status dpr_coalesced_plan_create(dpr_coalesced_plan** plan, int K, int P,
     pl->partition_numel = off;
     pl->n_tiles = tiles;
     pl->n_ag_tiles = ag_tiles;
+    // one block per reduce-scatter tile and per (all-gather tile, replica):
+    // both must fit a 1-D grid
+    if (tiles > int64_t(0x7FFFFFFF) || ag_tiles * K > int64_t(0x7FFFFFFF)) {
+        delete pl;
+        return DPR_ERR_UNSUPPORTED;
+    }
     cudaError_t e = cudaGetDevice(&pl->device);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (e == cudaSuccess && !pl->segs.empty()) {

@@ -205,3 +205,16 @@ def test_bf16_partition_rejections(L):
     assert c(ctypes.c_void_p(BASE), ctypes.c_void_p(BASE + 16), 16, None) == ALIAS
     assert c(None, None, 0, None) == OK
     assert c(ctypes.c_void_p(BASE), ctypes.c_void_p(BASE + 4096), -1, None) == INVALID
+
+
+def test_coalesced_plan_refuses_more_tiles_than_a_grid_holds(L):
+    """1000 parameters of 2^34 elements at K=64 need about 4.2e9 reduce-scatter
+    tiles of 4096 elements, more than a 1-D grid holds: refused on the host
+    (fake, non-overlapping addresses; nothing is dereferenced or allocated)."""
+    K, P = 64, 1000
+    n = 1 << 34
+    numel = (ctypes.c_int64 * P)(*([n] * P))
+    t = _arr([BASE + i * (1 << 35) for i in range(K * P)])
+    h = ctypes.c_void_p()
+    assert L.dpr_coalesced_plan_create(ctypes.byref(h), K, P, t, numel, None) == UNSUP
+    assert h.value is None
