@@ -12,7 +12,6 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import bf16 as obf
 from oracle import ring
 from workloads import synthetic as syn
 
@@ -100,26 +99,3 @@ def oracle_ar_sampled(at_fn, K: int, S: int, T: np.ndarray, mode: int, scale: fl
         x = gather_inputs(at_fn, K, 1, S, T)
     outs, _ = ring.allreduce(x[:K], K, mode, scale)
     return outs           # each: K chunks of |T|, chunk by chunk
-
-
-def device_slab_positions(t: torch.Tensor, base: int, T: np.ndarray) -> torch.Tensor:
-    idx = torch.from_numpy(T + base).to(t.device)
-    return t.index_select(0, idx).cpu()
-
-
-def fresh(*shape, dtype, dev, fill=None):
-    t = torch.empty(*shape, dtype=dtype, device=dev)
-    if fill is not None:
-        t.fill_(fill)
-    return t
-
-
-def widen_init(K: int, S: int, key_base: int, dev):
-    """Deterministic fp32 initial partition gradients (for accumulate tests):
-    bf16 generator values widened to fp32 -- identical on host and device."""
-    return [syn.gauss_bf16(0, S, syn.stream_key(key_base, j), 1e-2, device=dev).float()
-            for j in range(K)]
-
-
-def f32_of_bf16_bits(b: np.ndarray) -> np.ndarray:
-    return obf.to_f32(b)

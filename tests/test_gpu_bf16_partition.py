@@ -6,7 +6,6 @@ import pytest
 import torch
 
 import gradient_reduction_gb300 as dpr
-from oracle import bf16 as obf
 from oracle import ring
 from tests import gpu_helpers as H
 from tests.test_gpu_collectives import _inputs, _upload

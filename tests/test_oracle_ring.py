@@ -1,9 +1,7 @@
 """Pins of the CPU oracle's ring simulation against what the pages and the
 mathematics fix: the printed worked examples (round by round), closed forms,
 traffic counts, invariants, error bounds and exact-rational brute force."""
-import itertools
 import random
-from fractions import Fraction
 
 import numpy as np
 import pytest
