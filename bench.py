@@ -129,6 +129,18 @@ def job_value(bytes_per_step: float, steps: int, world: int, max_seconds: float)
 
 # ---- measurement helpers ---------------------------------------------------------
 
+def ring_busbw(kernel: str, K: int, N: int, seconds: float):
+    """Ring-equivalent bus bandwidth in GB/s, the collective libraries' figure
+    (CMU 11-868 Lecture 14 notes, section 3.4): a ring reduce-scatter or
+    all-gather of N elements per rank moves (K-1)/K of the N-element message
+    per rank, a ring all-reduce twice that.  None for the bucket gather."""
+    hops = {"rs": 1, "allgather": 1, "allreduce": 2}
+    key = "rs" if kernel.startswith("rs_") else kernel
+    if key not in hops:
+        return None
+    return hops[key] * (K - 1) / K * 2 * N / seconds / 1e9
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -698,6 +710,10 @@ def run_device(args, rank, world, local_rank):
         kernels_out[name] = {"bytes_per_launch": wl.bytes[name], "avg_ms": avg * 1e3,
                              "gbs": wl.bytes[name] / avg / 1e9, "launches": len(ts),
                              "time_share": sum(ts) / sum(sum(v) for v in per.values())}
+        if name in STEP_KERNELS:
+            bb = ring_busbw(name, wl.K, wl.N, avg)
+            if bb is not None:
+                kernels_out[name]["busbw_ring_equivalent_gbs"] = bb
     e2e = None
     if not args.no_e2e and not args.only and args.workload == "zero_bucket":
         e2e = run_e2e(wl, args, step_bytes)

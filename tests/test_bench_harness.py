@@ -78,3 +78,21 @@ def test_reference_arm_other_ranks_exit_quietly():
                           "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
                          cwd=ROOT, env=env, timeout=300)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("K", [2, 4, 8])
+def test_ring_busbw_matches_the_ring_simulation_traffic(K):
+    """The bus bandwidth figure times the launch time equals the bf16 bytes one
+    rank sends in the oracle's ring simulation of the same collective."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    from oracle import ring
+    N, t = 4 * K, 0.5
+    x = [np.zeros(N, np.uint16) for _ in range(K)]
+    sent = {"rs_fp32_m2": ring.reduce_scatter(x, K)[1].sent[0],
+            "allgather": ring.allgather([np.zeros(N // K, np.uint16)] * K, K)[1].sent[0],
+            "allreduce": ring.allreduce(x, K)[1].sent[0]}
+    for name, elems in sent.items():
+        assert bench.ring_busbw(name, K, N, t) * t * 1e9 == pytest.approx(2 * elems)
+    assert bench.ring_busbw("flatten", K, N, t) is None

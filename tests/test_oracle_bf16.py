@@ -1,8 +1,10 @@
 """Pins of the oracle's bf16 conversions against PyTorch's CPU bf16 conversion
 (a library routine) and against exact rational rounding."""
+import os
 import random
 
 import numpy as np
+import pytest
 import torch
 
 from oracle import bf16 as obf
@@ -73,3 +75,58 @@ def test_bf16_add_is_correctly_rounded_sum():
     for i in range(n):
         want = X.bf16(X.of_bf16_bits(a[i]) + X.of_bf16_bits(b[i]))
         assert X.same(X.of_bf16_bits(got[i]), want), (hex(a[i]), hex(b[i]))
+
+
+def _build_exhaustive(tmp_path, *defines):
+    """Compiles tests/bf16_add_exhaustive.c with the host C compiler (OpenMP
+    when available); skips where there is none."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = os.path.join(os.path.dirname(__file__), "bf16_add_exhaustive.c")
+    exe = str(tmp_path / ("bf16x" + "".join(d.lower() for d in defines)))
+    base = [cc, "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", *defines,
+            src, "-o", exe]
+    if subprocess.run(base[:1] + ["-fopenmp"] + base[1:], capture_output=True).returncode:
+        subprocess.run(base, check=True, capture_output=True)
+    return exe
+
+
+def _run(exe, *args):
+    import subprocess
+    out = subprocess.run([exe, *map(str, args)], capture_output=True, text=True, timeout=600,
+                         check=True).stdout
+    kv = dict(f.split("=") for f in out.split())
+    return int(kv["pairs"]), int(kv["mismatches"])
+
+
+def test_bf16_add_rule_exhaustive_over_all_pairs(tmp_path):
+    """Every one of the 2**32 (a, b) bf16 pairs: rounding the binary32 sum to
+    bf16 gives the exactly rounded bf16 sum (the per-hop rounding rule),
+    including zeros, subnormals, infinities and NaN.  The same checker built
+    with truncation in place of rounding must find mismatches."""
+    pairs, bad = _run(_build_exhaustive(tmp_path))
+    assert pairs == 1 << 32 and bad == 0
+    pairs, bad = _run(_build_exhaustive(tmp_path, "-DROUTE1_TRUNCATES"), 0x3F80, 0x3FC0)
+    assert pairs == 64 << 16 and bad > 0
+
+
+def test_oracle_add_equals_exact_rounding_for_every_b(tmp_path):
+    """The oracle's bf16 add against the checker's exact integer route, for
+    every b and first operands spread over signs, binades, subnormals and the
+    largest finite values."""
+    import subprocess
+    exe = _build_exhaustive(tmp_path)
+    a_list = [0x0000, 0x0001, 0x007F, 0x0080, 0x0081, 0x0100, 0x1234, 0x3F80, 0x3F81,
+              0x3FFF, 0x4000, 0x42C8, 0x5F00, 0x7F00, 0x7F7E, 0x7F7F, 0x7F80,
+              0x8000, 0x8001, 0x80FF, 0xBF80, 0xC000, 0xC2C8, 0xFF7F, 0xFF80]
+    raw = subprocess.run([exe, "--dump", *map(str, a_list)], capture_output=True, timeout=300,
+                         check=True).stdout
+    want = np.frombuffer(raw, dtype="<u2").reshape(len(a_list), 65536)
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    for i, a in enumerate(a_list):
+        with np.errstate(invalid="ignore"):         # inf + -inf
+            got = obf.add(np.full(65536, a, np.uint16), b)
+        assert np.array_equal(got, want[i]), hex(a)
