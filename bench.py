@@ -23,8 +23,8 @@ roofline = the dominant kernel's algorithmic bytes per launch / its average
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dpr|reference]
 
---impl reference times the CPU oracle (numpy, host cores) on a bounded sample
-of the same workload.  With --gpus N > 1 (under torchrun) every rank runs an
+--impl reference times the CPU oracle (numpy, one process per host core, each
+on its own slab) on a bounded sample of the same workload.  With --gpus N > 1 (under torchrun) every rank runs an
 independent replica of the workload on its own GPU (the path does not shard
 across GPUs); the job value is the bytes of all ranks over the slowest rank's
 time.
@@ -810,24 +810,47 @@ class OracleSample:
     """The bench workload scaled down for the CPU oracle: same K and fragment
     count, N_s elements per rank."""
 
-    def __init__(self, n_per_rank: int):
+    ARRAYS = ("frags", "ipg0", "part", "shards")
+
+    def __init__(self, n_per_rank: int, arrays: dict | None = None):
         from workloads import configs as C
-        from workloads import synthetic as syn
         w = C.BENCH
         self.K = K = w.K
         self.P = P = w.n_frag
         self.N = N = n_per_rank
         self.F = F = N // P
         self.S = S = N // K
-        bits = syn.bf16_bits
-        self.frags = [[bits(w.dist.fill(0, F, w.frag_key(r, p))) for p in range(P)]
-                      for r in range(K)]
-        self.ipg0 = [bits(w.dist.fill(0, N, w.micro0_key(r))) for r in range(K)]
-        self.part = [syn.gauss_bf16(0, S, w.prev_grad_key(j), 1e-3).float().numpy()
-                     for j in range(K)]
-        self.shards = [bits(w.param_dist.fill(j * S, S, w.param_key())) for j in range(K)]
+        if arrays is None:
+            from workloads import synthetic as syn
+            bits = syn.bf16_bits
+            import numpy as np
+            arrays = {
+                "frags": np.stack([np.stack([bits(w.dist.fill(0, F, w.frag_key(r, p)))
+                                             for p in range(P)]) for r in range(K)]),
+                "ipg0": np.stack([bits(w.dist.fill(0, N, w.micro0_key(r))) for r in range(K)]),
+                "part": np.stack([syn.gauss_bf16(0, S, w.prev_grad_key(j), 1e-3).float().numpy()
+                                  for j in range(K)]),
+                "shards": np.stack([bits(w.param_dist.fill(j * S, S, w.param_key()))
+                                    for j in range(K)]),
+            }
+        self.arrays = arrays
+        self.frags = [list(arrays["frags"][r]) for r in range(K)]
+        self.ipg0 = list(arrays["ipg0"])
+        self.part = list(arrays["part"])
+        self.shards = list(arrays["shards"])
         self.bytes = 4 * K * N + (4 * K * N + 4 * N) + (4 * K * N + 8 * N) + (2 * N + 2 * K * N) \
             + 4 * K * N
+
+    def save(self, folder: str):
+        import numpy as np
+        for name in self.ARRAYS:
+            np.save(os.path.join(folder, name + ".npy"), self.arrays[name])
+
+    @classmethod
+    def load(cls, folder: str, n_per_rank: int):
+        import numpy as np
+        return cls(n_per_rank, {name: np.load(os.path.join(folder, name + ".npy"))
+                                for name in cls.ARRAYS})
 
     def step(self):
         from oracle import flatten as ofl
@@ -839,6 +862,80 @@ class OracleSample:
         ring.reduce_scatter(x, K, 2, ring.HOP_BF16, 1.0 / K, out_init=self.part)
         ring.allgather(self.shards, K)
         ring.allreduce(flat, K, ring.RING_FP32, 1.0 / K)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _slab_worker(folder, n, barrier, cmds):
+    """One oracle process: every element position of the workload is
+    independent, so each core runs the whole oracle on its own slab.  Waits at
+    the barrier, runs the commanded number of passes, waits again."""
+    smp = OracleSample.load(folder, n)
+    smp.step()                                  # warm-up
+    while True:
+        passes = cmds.get()
+        if passes is None:
+            return
+        barrier.wait()
+        for _ in range(passes):
+            smp.step()
+        barrier.wait()
+
+
+class OracleSlabPool:
+    """`cores` spawned processes, each holding one slab (a K=8 sample of n
+    elements per rank) of the bench workload and running the oracle on it.
+    run(p) times p passes of every process, from a common start to the last
+    one's end.  Processes are started with spawn: none inherits the parent's
+    CUDA state."""
+
+    def __init__(self, n: int, cores: int):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.n, self.cores = n, cores
+        self.folder = tempfile.mkdtemp(prefix="oracle_slab_")
+        smp = OracleSample(n)
+        smp.save(self.folder)
+        self.bytes = smp.bytes
+        del smp
+        self.barrier = ctx.Barrier(cores + 1)
+        self.cmds = [ctx.Queue() for _ in range(cores)]
+        env_before = os.environ.get("OMP_NUM_THREADS")
+        os.environ["OMP_NUM_THREADS"] = "1"     # one thread per process
+        try:
+            self.procs = [ctx.Process(target=_slab_worker,
+                                      args=(self.folder, n, self.barrier, q), daemon=True)
+                          for q in self.cmds]
+            for pr in self.procs:
+                pr.start()
+        finally:
+            if env_before is None:
+                os.environ.pop("OMP_NUM_THREADS", None)
+            else:
+                os.environ["OMP_NUM_THREADS"] = env_before
+
+    def run(self, passes: int) -> float:
+        for q in self.cmds:
+            q.put(passes)
+        self.barrier.wait(timeout=600)
+        t0 = time.perf_counter()
+        self.barrier.wait(timeout=600)
+        return time.perf_counter() - t0
+
+    def close(self):
+        import shutil
+        for q in self.cmds:
+            q.put(None)
+        for pr in self.procs:
+            pr.join(timeout=30)
+            if pr.is_alive():
+                pr.kill()
+        shutil.rmtree(self.folder, ignore_errors=True)
 
 
 def time_oracle(n_per_rank: int, min_seconds: float, min_steps: int = 1):
@@ -853,12 +950,27 @@ def time_oracle(n_per_rank: int, min_seconds: float, min_steps: int = 1):
 
 
 def cpu_baseline(args):
+    """The oracle on every host core (one slab per process), with the
+    single-thread figure beside it."""
     n = 1 << 20
-    smp, steps, el = time_oracle(n, args.cpu_seconds)
-    return {"value": round(smp.bytes * steps / el / 1e9, 4), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
-            "sample": f"K=8, {n} elements per rank (32 fragments of {n // 32}), the same five "
-                      f"steps, {steps} passes in {el:.1f} s, numpy single thread"}
+    smp, steps1, el1 = time_oracle(n, args.cpu_seconds / 2)
+    one = smp.bytes * steps1 / el1 / 1e9
+    del smp
+    cores = host_cores()
+    pool = OracleSlabPool(n, cores)
+    try:
+        t1 = pool.run(1)
+        passes = max(1, round(args.cpu_seconds / 2 / t1))
+        el = pool.run(passes)
+    finally:
+        pool.close()
+    value = pool.bytes * cores * passes / el / 1e9
+    return {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "single_core_value": round(one, 4),
+            "sample": f"K=8, the same five steps; {cores} processes, each running the oracle "
+                      f"(numpy, one thread) on its own slab of {n} elements per rank (32 "
+                      f"fragments of {n // 32}), {passes} passes in {el:.1f} s; one process "
+                      f"alone: {steps1} passes in {el1:.1f} s"}
 
 
 def common_config(world):
@@ -871,18 +983,21 @@ def common_config(world):
 
 
 def run_reference(args):
+    """The reference arm: the oracle on every host core, one slab per process,
+    each step one pass of every process over its slab."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     n = 1 << 18
-    smp = OracleSample(n)
-    for _ in range(args.warmup):
-        smp.step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        smp.step()
-    el = time.perf_counter() - t0
-    value = smp.bytes * args.steps / el / 1e9
+    cores = host_cores()
+    pool = OracleSlabPool(n, cores)
+    try:
+        for _ in range(args.warmup):
+            pool.run(1)
+        el = sum(pool.run(1) for _ in range(args.steps))
+    finally:
+        pool.close()
+    value = pool.bytes * cores * args.steps / el / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -890,9 +1005,10 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate",
         "data": "synthetic (seeded counter-hash generator)",
         "config": common_config(1),
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"K=8, {n} elements per rank (32 fragments of {n // 32}), "
-                                   "the same five steps per step, numpy single thread"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"K=8, the same five steps per step; {cores} processes, each "
+                                   f"running the oracle (numpy, one thread) on its own slab of "
+                                   f"{n} elements per rank (32 fragments of {n // 32})"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
