@@ -64,6 +64,13 @@ NCU_TRAFFIC = {
     "rs_hop_m2_acc": {"bytes": 21_460_000_000, "src_sha": "7e627fc3de0cef69"},
     "allgather": {"bytes": 9_601_000_000, "src_sha": "81b7d453ae3c43eb"},
     "allreduce": {"bytes": 17_123_000_000, "src_sha": "7e627fc3de0cef69"},
+    # the same metrics on the other workloads' first timed step
+    # (profiles/zero3_and_bf16_partition_dram_traffic.md)
+    "rs_coalesced": {"bytes": 22_004_000_000, "src_sha": "a947686bcfd68570"},
+    "ag_coalesced": {"bytes": 19_755_000_000, "src_sha": "89f935c89cda9999"},
+    "rs_bf16_copy": {"bytes": 9_653_000_000, "src_sha": "7e627fc3de0cef69"},
+    "rs_bf16_add": {"bytes": 10_725_000_000, "src_sha": "7e627fc3de0cef69"},
+    "cast": {"bytes": 3_163_000_000, "src_sha": "154661a8917e772d"},
 }
 
 
@@ -160,6 +167,11 @@ KERNEL_SOURCES = {
     "rs_fp32_m2": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
     "rs_hop_m2_acc": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
     "allreduce": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
+    "rs_coalesced": ["coalesced.cu", "dpr_ring.cuh", "dpr_device.cuh", "dpr_kernels.h"],
+    "ag_coalesced": ["coalesced.cu", "dpr_device.cuh", "dpr_kernels.h"],
+    "rs_bf16_copy": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
+    "rs_bf16_add": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
+    "cast": ["reduce_kernels.cu"] + _COMMON_SRC,
 }
 
 

@@ -13,7 +13,9 @@
 //
 // Work is cut into (parameter, shard) segments and tiles of kCoalTile
 // elements; one block handles one tile (and, for the all-gather, one
-// replica), finding its segment by binary search over first-tile indices.
+// replica).  A per-tile map gives each block its segment and parameter in one
+// load, so the segment record and the tensor pointers arrive together, two
+// dependent loads before the first data load.
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -41,10 +43,15 @@ struct CoalSeg {
     int32_t pad;
 };
 
+struct TileRef {
+    int32_t seg;      // segment of the tile
+    int32_t p;        // its parameter (= segs[seg].p, here so the pointer load need not wait)
+};
+
 struct CoalParams {
     const CoalSeg* segs;
+    const TileRef* tiles;           // reduce-scatter tiles, or all-gather tiles
     uint16_t* const* ptrs;          // device table [K * P]: tensors[r * P + p]
-    int64_t n_seg;
     int64_t n_tiles;
     float* out[DPR_MAX_RANKS];      // reduce-scatter: fp32 partitions
     const uint16_t* shard[DPR_MAX_RANKS];   // all-gather: bf16 partitions
@@ -55,24 +62,17 @@ struct CoalParams {
     int bases_aligned32;            // every out / shard base is 32-byte aligned
 };
 
-template <bool AG>
-__device__ __forceinline__ int64_t find_segment(const CoalSeg* segs, int64_t n_seg, int64_t tile) {
-    int64_t lo = 0, hi = n_seg - 1;
-    while (lo < hi) {
-        const int64_t mid = (lo + hi + 1) >> 1;
-        if ((AG ? segs[mid].ag_tile0 : segs[mid].tile0) <= tile) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
-template <int MODE>
+// KC > 0: K = KC fixed at compile time (the ring's loads and adds unrolled,
+// about half the registers of the run-time-K form); KC == 0: any K.
+template <int KC, int MODE>
 __global__ void __launch_bounds__(kThreads) rs_coalesced(const __grid_constant__ CoalParams p) {
     __shared__ const uint16_t* base[DPR_MAX_RANKS];
     const int64_t tile = blockIdx.x;
-    const CoalSeg sg = p.segs[find_segment<false>(p.segs, p.n_seg, tile)];
-    const int K = p.K;
-    if (threadIdx.x < K) base[threadIdx.x] = p.ptrs[int64_t(threadIdx.x) * p.P + sg.p] + sg.j * sg.s;
+    const TileRef tr = p.tiles[tile];
+    const int K = KC > 0 ? KC : p.K;
+    const uint16_t* t = (threadIdx.x < K) ? p.ptrs[int64_t(threadIdx.x) * p.P + tr.p] : nullptr;
+    const CoalSeg sg = p.segs[tr.seg];
+    if (threadIdx.x < K) base[threadIdx.x] = t + sg.j * sg.s;
     __syncthreads();
     const int64_t t0 = (tile - sg.tile0) * kCoalTile;
     const int64_t n = (sg.s - t0 < kCoalTile) ? sg.s - t0 : kCoalTile;
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) rs_coalesced(const __grid_constant__
         // whole tile inside the parameter: 16 elements per thread and access
         for (int64_t u = threadIdx.x; u < n / 16; u += kThreads) {
             float acc[16];
-            ring_sum<0, 1, MODE, 8, true>(base, K, sg.j, uint64_t(t0 + 16 * u), acc);
+            ring_sum<KC, 1, MODE, 8, true>(base, K, sg.j, uint64_t(t0 + 16 * u), acc);
             store_shard<8>(out + 16 * u, acc, p.scale, p.accumulate);
         }
         return;
@@ -113,12 +113,14 @@ __global__ void __launch_bounds__(kThreads) ag_coalesced(const __grid_constant__
     const uint64_t b = blockIdx.x;
     const int r = int(b % uint64_t(p.K));
     const int64_t tile = int64_t(b / uint64_t(p.K));
-    const CoalSeg sg = p.segs[find_segment<true>(p.segs, p.n_seg, tile)];
+    const TileRef tr = p.tiles[tile];
+    uint16_t* const t = p.ptrs[int64_t(r) * p.P + tr.p];
+    const CoalSeg sg = p.segs[tr.seg];
     const int64_t t0 = (tile - sg.ag_tile0) * kCoalAgTile;
     const int64_t n = (sg.valid - t0 < kCoalAgTile) ? sg.valid - t0 : kCoalAgTile;
     if (n <= 0) return;
     const uint16_t* src = p.shard[sg.j] + sg.off + t0;
-    uint16_t* dst = p.ptrs[int64_t(r) * p.P + sg.p] + sg.j * sg.s + t0;
+    uint16_t* dst = t + sg.j * sg.s + t0;
     if (sg.vec && p.bases_aligned32 && n == kCoalAgTile) {
 #pragma unroll
         for (int u = 0; u < int(kCoalAgTile) / 16 / kThreads; ++u) {
@@ -135,6 +137,19 @@ __global__ void __launch_bounds__(kThreads) ag_coalesced(const __grid_constant__
 struct Span {
     uintptr_t lo, hi;
 };
+
+template <int MODE>
+const void* rs_coalesced_for(int K) {
+    switch (K) {
+        case 2: return reinterpret_cast<const void*>(rs_coalesced<2, MODE>);
+        case 4: return reinterpret_cast<const void*>(rs_coalesced<4, MODE>);
+        case 8: return reinterpret_cast<const void*>(rs_coalesced<8, MODE>);
+        case 16: return reinterpret_cast<const void*>(rs_coalesced<16, MODE>);
+        case 32: return reinterpret_cast<const void*>(rs_coalesced<32, MODE>);
+        case 64: return reinterpret_cast<const void*>(rs_coalesced<64, MODE>);
+        default: return reinterpret_cast<const void*>(rs_coalesced<0, MODE>);
+    }
+}
 
 bool overlap(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; }
 
@@ -158,8 +173,30 @@ struct dpr_coalesced_plan {
     std::vector<CoalSeg> segs;
     std::vector<Span> tensor_spans;
     CoalSeg* d_segs = nullptr;
+    TileRef* d_tiles = nullptr;      // [n_tiles]
+    TileRef* d_ag_tiles = nullptr;   // [n_ag_tiles]
     uint16_t** d_ptrs = nullptr;
 };
+
+namespace {
+
+void free_plan(dpr_coalesced_plan* pl) {
+    if (pl->d_segs) cudaFree(pl->d_segs);
+    if (pl->d_tiles) cudaFree(pl->d_tiles);
+    if (pl->d_ag_tiles) cudaFree(pl->d_ag_tiles);
+    if (pl->d_ptrs) cudaFree(pl->d_ptrs);
+    delete pl;
+}
+
+template <typename T>
+cudaError_t upload(T** dst, const std::vector<T>& src, cudaStream_t st) {
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), src.size() * sizeof(T));
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice, st);
+    return e;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -224,27 +261,29 @@ dpr_status dpr_coalesced_plan_create(dpr_coalesced_plan** plan, int K, int P,
     // one block per reduce-scatter tile and per (all-gather tile, replica):
     // both must fit a 1-D grid
     if (tiles > int64_t(0x7FFFFFFF) || ag_tiles * K > int64_t(0x7FFFFFFF)) {
-        delete pl;
+        free_plan(pl);
         return DPR_ERR_UNSUPPORTED;
     }
     cudaError_t e = cudaGetDevice(&pl->device);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (e == cudaSuccess && !pl->segs.empty()) {
-        e = cudaMalloc(reinterpret_cast<void**>(&pl->d_segs), pl->segs.size() * sizeof(CoalSeg));
-        if (e == cudaSuccess)
-            e = cudaMalloc(reinterpret_cast<void**>(&pl->d_ptrs), size_t(K) * P * sizeof(uint16_t*));
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(pl->d_segs, pl->segs.data(), pl->segs.size() * sizeof(CoalSeg),
-                                cudaMemcpyHostToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(pl->d_ptrs, tensors, size_t(K) * P * sizeof(uint16_t*),
-                                cudaMemcpyHostToDevice, st);
+        std::vector<TileRef> map(static_cast<size_t>(tiles)), ag_map(static_cast<size_t>(ag_tiles));
+        for (size_t g = 0; g < pl->segs.size(); ++g) {
+            const CoalSeg& sg = pl->segs[g];
+            const TileRef ref{int32_t(g), sg.p};
+            std::fill_n(map.begin() + sg.tile0, (sg.s + kCoalTile - 1) / kCoalTile, ref);
+            std::fill_n(ag_map.begin() + sg.ag_tile0, (sg.s + kCoalAgTile - 1) / kCoalAgTile, ref);
+        }
+        std::vector<uint16_t*> ptrs(size_t(K) * P);
+        for (size_t i = 0; i < ptrs.size(); ++i) ptrs[i] = static_cast<uint16_t*>(tensors[i]);
+        e = upload(&pl->d_segs, pl->segs, st);
+        if (e == cudaSuccess) e = upload(&pl->d_tiles, map, st);
+        if (e == cudaSuccess) e = upload(&pl->d_ag_tiles, ag_map, st);
+        if (e == cudaSuccess) e = upload(&pl->d_ptrs, ptrs, st);
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     }
     if (e != cudaSuccess) {
-        if (pl->d_segs) cudaFree(pl->d_segs);
-        if (pl->d_ptrs) cudaFree(pl->d_ptrs);
-        delete pl;
+        free_plan(pl);
         return coal_cuda(e);
     }
     *plan = pl;
@@ -285,8 +324,8 @@ dpr_status dpr_reduce_scatter_coalesced(const dpr_coalesced_plan* plan, float* c
     CoalParams prm;
     std::memset(&prm, 0, sizeof(prm));
     prm.segs = plan->d_segs;
+    prm.tiles = plan->d_tiles;
     prm.ptrs = plan->d_ptrs;
-    prm.n_seg = int64_t(plan->segs.size());
     prm.n_tiles = plan->n_tiles;
     for (int j = 0; j < K; ++j) prm.out[j] = out[j];
     prm.K = K;
@@ -294,9 +333,8 @@ dpr_status dpr_reduce_scatter_coalesced(const dpr_coalesced_plan* plan, float* c
     prm.scale = scale;
     prm.accumulate = accumulate ? 1 : 0;
     prm.bases_aligned32 = a32 ? 1 : 0;
-    const void* k = (mode == DPR_SUM_RING_FP32)
-                        ? reinterpret_cast<const void*>(rs_coalesced<DPR_SUM_RING_FP32>)
-                        : reinterpret_cast<const void*>(rs_coalesced<DPR_SUM_HOP_BF16>);
+    const void* k = (mode == DPR_SUM_RING_FP32) ? rs_coalesced_for<DPR_SUM_RING_FP32>(K)
+                                                : rs_coalesced_for<DPR_SUM_HOP_BF16>(K);
     void* args[] = {&prm};
     return coal_cuda(cudaLaunchKernel(k, dim3(unsigned(plan->n_tiles)), dim3(kThreads), args, 0,
                                       static_cast<cudaStream_t>(stream)));
@@ -324,9 +362,9 @@ dpr_status dpr_allgather_coalesced(const dpr_coalesced_plan* plan, const void* c
     CoalParams prm;
     std::memset(&prm, 0, sizeof(prm));
     prm.segs = plan->d_segs;
+    prm.tiles = plan->d_ag_tiles;
     prm.ptrs = plan->d_ptrs;
-    prm.n_seg = int64_t(plan->segs.size());
-    prm.n_tiles = plan->n_tiles;
+    prm.n_tiles = plan->n_ag_tiles;
     for (int j = 0; j < K; ++j) prm.shard[j] = static_cast<const uint16_t*>(shards[j]);
     prm.K = K;
     prm.P = plan->P;
@@ -341,11 +379,15 @@ dpr_status dpr_allgather_coalesced(const dpr_coalesced_plan* plan, const void* c
 dpr_status dpr_coalesced_plan_destroy(dpr_coalesced_plan* plan) {
     if (!plan) return DPR_OK;
     cudaError_t e = cudaSuccess;
-    if (plan->d_segs) e = cudaFree(plan->d_segs);
-    if (plan->d_ptrs) {
-        cudaError_t e2 = cudaFree(plan->d_ptrs);
+    for (void* q : {static_cast<void*>(plan->d_segs), static_cast<void*>(plan->d_tiles),
+                    static_cast<void*>(plan->d_ag_tiles), static_cast<void*>(plan->d_ptrs)}) {
+        if (!q) continue;
+        const cudaError_t e2 = cudaFree(q);
         if (e == cudaSuccess) e = e2;
     }
+    plan->d_segs = nullptr;
+    plan->d_tiles = plan->d_ag_tiles = nullptr;
+    plan->d_ptrs = nullptr;
     delete plan;
     return coal_cuda(e);
 }

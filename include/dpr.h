@@ -227,7 +227,8 @@ dpr_status dpr_flatten_bucket_noalloc(int K, int P, const void* const* src, cons
  * dpr_coalesced_plan_create binds the K*P per-rank tensors (gradients for the
  * reduce-scatter, parameters for the all-gather; tensors[r*P + p] = rank r's
  * tensor of parameter p, bf16, numel[p] elements, non-overlapping) and
- * uploads a segment table and the pointer table once (cudaMalloc; waits for
+ * uploads a segment table, a per-tile map and the pointer table once
+ * (cudaMalloc, about 8 bytes per 4096 gradient elements of one rank; waits for
  * the upload).  numel[p] == 0 is allowed.
  *
  * dpr_reduce_scatter_coalesced: out[j][offset_p + t] = scale * (ring-order
