@@ -81,6 +81,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["dpr", "reference"], default="dpr")
     p.add_argument("--e2e-steps", type=int, default=8)
+    p.add_argument("--pg-timeout", type=float, default=600.0,
+                   help="seconds before a collective of the multi-rank harness gives up on "
+                        "a rank that has gone")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -108,6 +111,19 @@ def dist_env():
     """(rank, world, local_rank) from torchrun's environment."""
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(backend: str, device=None, timeout_s: float = 600.0):
+    """Process group over torchrun's environment.  A rank that dies between
+    steps makes the others' next barrier or reduction end with an error
+    within timeout_s instead of waiting forever."""
+    import datetime
+
+    import torch.distributed as dist
+    kw = {"timeout": datetime.timedelta(seconds=timeout_s)}
+    if device is not None:
+        kw["device_id"] = device
+    dist.init_process_group(backend, **kw)
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -1039,8 +1055,7 @@ def main(argv=None):
     import torch
     rank, world, local_rank = dist_env()
     if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        init_dist("nccl", torch.device("cuda", local_rank), args.pg_timeout)
     res = run_device(args, rank, world, local_rank)
     peak, peak_kind = load_peaks()
     kern = res["kernels"]

@@ -53,6 +53,43 @@ def test_two_rank_harness_gloo():
         assert val == pytest.approx(1e9 * 10 * 2 / 2.0 / 1e9)
 
 
+def _dying_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import time
+    import bench
+    bench.init_dist("gloo", timeout_s=5.0)
+    if rank == 1:
+        os._exit(3)                  # leaves between steps, nothing of its own in flight
+    t0 = time.monotonic()
+    try:
+        bench.barrier()
+        q.put(("no error", time.monotonic() - t0))
+    except Exception as e:           # noqa: BLE001 - any error is the detection
+        q.put((type(e).__name__, time.monotonic() - t0))
+    q.close()
+    q.join_thread()
+    os._exit(0)
+
+
+def test_rank_that_leaves_ends_the_next_barrier_with_an_error():
+    """A rank that exits between steps: the other rank's next barrier raises
+    within the process-group timeout instead of waiting for it forever."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dying_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    what, waited = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=60)
+    assert what != "no error"
+    assert waited < 60
+    assert procs[0].exitcode == 0 and procs[1].exitcode == 3
+
+
 def test_job_value_single():
     sys.path.insert(0, ROOT)
     import bench
