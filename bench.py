@@ -59,18 +59,18 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum at the bench's full size
     # (K=8, N=2**29), one launch each (profiles/step_k8_1GiB_dram_traffic.md); src_sha is
     # kernel_src_sha(kernel) of the sources the capture was taken from
-    "flatten": {"bytes": 17_128_000_000, "src_sha": "81b7d453ae3c43eb"},
-    "rs_fp32_m2": {"bytes": 19_314_000_000, "src_sha": "7e627fc3de0cef69"},
-    "rs_hop_m2_acc": {"bytes": 21_460_000_000, "src_sha": "7e627fc3de0cef69"},
-    "allgather": {"bytes": 9_601_000_000, "src_sha": "81b7d453ae3c43eb"},
-    "allreduce": {"bytes": 17_123_000_000, "src_sha": "7e627fc3de0cef69"},
+    "flatten": {"bytes": 17_129_000_000, "src_sha": "81b7d453ae3c43eb"},
+    "rs_fp32_m2": {"bytes": 19_312_000_000, "src_sha": "f0c947c43bd74401"},
+    "rs_hop_m2_acc": {"bytes": 21_459_000_000, "src_sha": "f0c947c43bd74401"},
+    "allgather": {"bytes": 9_600_000_000, "src_sha": "81b7d453ae3c43eb"},
+    "allreduce": {"bytes": 17_122_000_000, "src_sha": "f0c947c43bd74401"},
     # the same metrics on the other workloads' first timed step
     # (profiles/zero3_and_bf16_partition_dram_traffic.md)
     "rs_coalesced": {"bytes": 22_004_000_000, "src_sha": "a947686bcfd68570"},
     "ag_coalesced": {"bytes": 19_755_000_000, "src_sha": "89f935c89cda9999"},
-    "rs_bf16_copy": {"bytes": 9_653_000_000, "src_sha": "7e627fc3de0cef69"},
-    "rs_bf16_add": {"bytes": 10_725_000_000, "src_sha": "7e627fc3de0cef69"},
-    "cast": {"bytes": 3_163_000_000, "src_sha": "154661a8917e772d"},
+    "rs_bf16_copy": {"bytes": 9_654_000_000, "src_sha": "f0c947c43bd74401"},
+    "rs_bf16_add": {"bytes": 10_725_000_000, "src_sha": "f0c947c43bd74401"},
+    "cast": {"bytes": 3_163_000_000, "src_sha": "b5d5cff3cb193264"},
 }
 
 
@@ -89,7 +89,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--workload", choices=["zero_bucket", "zero3_per_param", "bucket_pipeline",
-                                          "bf16_partition", "sweep"],
+                                          "bf16_partition", "sweep", "configs"],
                    default="zero_bucket",
                    help="zero_bucket: the headline step (default); zero3_per_param: the ZeRO-3 "
                         "discrete path on config 3's 56 gradients; bucket_pipeline: backward "
@@ -545,6 +545,150 @@ class PipelineBackward:
             p.close()
 
 
+class LaunchTimer:
+    """Average launch time of fn() on stream s (CUDA events).  Working sets
+    below 1 GiB are timed launch by launch with the L2 flushed before each
+    launch by reading 512 MiB, so no point is measured L2-resident (a read
+    leaves clean lines; a write-based flush would leave ~129 MB of dirty lines
+    whose write-back the timed kernel would pay for)."""
+
+    def __init__(self, s, steps: int, warmup: int):
+        import torch
+        self.torch, self.s, self.steps, self.warmup = torch, s, steps, warmup
+        self.flush = torch.ones(128 << 20, dtype=torch.int32, device=s.device)  # 512 MiB > L2
+
+    def __call__(self, fn, working_set: int) -> float:
+        torch, s = self.torch, self.s
+        torch.cuda.synchronize()
+        for _ in range(self.warmup):
+            fn()
+        s.synchronize()
+        if working_set >= (1 << 30):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(self.steps):
+                fn()
+            b.record(s)
+            s.synchronize()
+            return a.elapsed_time(b) / 1e3 / self.steps
+        ts = []
+        for _ in range(self.steps):
+            with torch.cuda.stream(s):
+                self.flush.sum()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            ts.append((a, b))
+        s.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ts) / 1e3 / len(ts)
+
+
+def run_configs_bench(args):
+    """Configurations 1 to 4 as the workload table states them, each timed
+    like the sweep (configuration 5): algorithmic bytes over the average time
+    of the listed launches.
+      1: K=4, N=4096: reduce-scatter ring fp32 x1/4 and all-reduce (launch-bound)
+      2: K=8, one 25M-element bucket per rank: reduce-scatter, both modes, x1/8
+      3: K=8, 56 fragmented gradients of a 7-layer hidden-4096 model: each
+         bucket gathered by offset table, then reduce-scattered (ring fp32) into
+         the fp32 partition; one figure for all buckets of a backward pass
+      4: K=8, all-gather of one hidden-8192 layer from 1/8 shards."""
+    import torch
+    import gradient_reduction_gb300 as dpr
+    from workloads import configs as C
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = torch.cuda.Stream(device=dev)
+    timed = LaunchTimer(s, args.steps, args.warmup)
+    bf, f32 = torch.bfloat16, torch.float32
+    rows = []
+
+    def row(cfg, op, nbytes, t, launches=1):
+        r = {"config": cfg, "op": op, "bytes": int(nbytes), "launches": launches,
+             "us": round(t * 1e6, 2), "gbs": round(nbytes / t / 1e9, 1)}
+        rows.append(r)
+        print(json.dumps(r), file=sys.stderr, flush=True)
+
+    with torch.cuda.stream(s):
+        # configuration 1
+        K, N = C.CFG1.K, C.CFG1.N
+        S = N // K
+        x = [C.CFG1.buffer(r, device=dev) for r in range(K)]
+        out = [torch.empty(S, dtype=f32, device=dev) for _ in range(K)]
+        ar = [torch.empty(N, dtype=bf, device=dev) for _ in range(K)]
+        t = timed(lambda: dpr.dpr_reduce_scatter(x, K, 1, N, out, mode=dpr.RING_FP32, stream=s),
+                  2 * K * N + 4 * N)
+        row(1, "rs_fp32", 2 * K * N + 4 * N, t)
+        t = timed(lambda: dpr.dpr_allreduce(x, K, N, ar, mode=dpr.RING_FP32, stream=s), 4 * K * N)
+        row(1, "allreduce", 4 * K * N, t)
+        del x, out, ar
+        # configuration 2
+        K, N = C.CFG2.K, C.CFG2.N
+        S = N // K
+        x = [C.CFG2.buffer(r, device=dev) for r in range(K)]
+        out = [torch.empty(S, dtype=f32, device=dev) for _ in range(K)]
+        for mode, name in ((dpr.RING_FP32, "rs_fp32"), (dpr.HOP_BF16, "rs_hop")):
+            t = timed(lambda: dpr.dpr_reduce_scatter(x, K, 1, N, out, mode=mode, stream=s),
+                      2 * K * N + 4 * N)
+            row(2, name, 2 * K * N + 4 * N, t)
+        del x, out
+        torch.cuda.empty_cache()
+        # configuration 3
+        cfg = C.CFG3
+        K = cfg.K
+        numel = [n for *_, n in cfg.arrival_order()]
+        bucket_of, offset, bucket_numel = dpr.dpr_bucket_assign(numel, cfg.bucket_cap, pad_to=8 * K)
+        grads = [[cfg.grad(r, p, device=dev) for p in range(len(numel))] for r in range(K)]
+        part = torch.empty(K, sum(bucket_numel) // K, dtype=f32, device=dev)
+        ipg = torch.zeros(K, max(bucket_numel), dtype=bf, device=dev)
+        steps = []
+        at = 0
+        for b, nb in enumerate(bucket_numel):
+            ps = [p for p in range(len(numel)) if bucket_of[p] == b]
+            plan = dpr.dpr_flatten_plan_create([[grads[r][p] for p in ps] for r in range(K)],
+                                               [numel[p] for p in ps], [offset[p] for p in ps],
+                                               nb, stream=s)
+            views = [ipg[r, :nb] for r in range(K)]
+            outs = [part[j, at:at + nb // K] for j in range(K)]
+            steps.append((plan, views, outs, nb))
+            at += nb // K
+
+        def backward():
+            for plan, views, outs, nb in steps:
+                dpr.dpr_flatten_bucket(plan, views, stream=s)
+                dpr.dpr_reduce_scatter(views, K, 1, nb, outs, mode=dpr.RING_FP32, stream=s)
+
+        total = sum(bucket_numel)
+        nbytes = 4 * K * total + 2 * K * total + 4 * total
+        t = timed(backward, nbytes)
+        row(3, "flatten+rs_fp32 per bucket", nbytes, t, launches=2 * len(steps))
+        for plan, *_ in steps:
+            plan.close()
+        del steps, grads, part, ipg
+        torch.cuda.empty_cache()
+        # configuration 4
+        K, N = C.CFG4.K, C.CFG4.N
+        S = N // K
+        shards = [C.cfg4_shard(j, device=dev) for j in range(K)]
+        full = [torch.empty(N, dtype=bf, device=dev) for _ in range(K)]
+        t = timed(lambda: dpr.dpr_allgather(shards, K, N, full, stream=s), 2 * N + 2 * K * N)
+        row(4, "allgather", 2 * N + 2 * K * N, t)
+        del shards, full
+        torch.cuda.empty_cache()
+    peak, kind = load_peaks()
+    head = [r for r in rows if r["config"] == 3][0]
+    line = {"metric": METRIC, "value": head["gbs"], "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "config": {"workload": "configs_1_to_4"},
+            "value_is": "configuration 3: gather + reduce-scatter of every bucket of one backward",
+            "peak": peak, "peak_kind": kind, "table": rows}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_sweep_bench(args):
     """Configuration 5's sweep: effective GB/s of the reduce-scatter (both
     modes, 2 micro-batches), all-gather and all-reduce for K in
@@ -558,39 +702,7 @@ def run_sweep_bench(args):
     torch.cuda.set_device(dev)
     s = torch.cuda.Stream(device=dev)
 
-    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)      # 512 MiB > L2 (129 MB)
-
-    def timed(fn, working_set):
-        """Average launch time.  Working sets below 1 GiB are timed launch by
-        launch with the L2 flushed before each launch by reading 512 MiB, so no
-        point is measured L2-resident (a read leaves clean lines; a write-based
-        flush would leave ~129 MB of dirty lines whose write-back the timed
-        kernel would pay for)."""
-        torch.cuda.synchronize()
-        for _ in range(args.warmup):
-            fn()
-        s.synchronize()
-        if working_set >= (1 << 30):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(s)
-            for _ in range(args.steps):
-                fn()
-            b.record(s)
-            s.synchronize()
-            return a.elapsed_time(b) / 1e3 / args.steps
-        ts = []
-        for _ in range(args.steps):
-            with torch.cuda.stream(s):
-                flush.sum()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(s)
-            fn()
-            b.record(s)
-            ts.append((a, b))
-        s.synchronize()
-        return sum(a.elapsed_time(b) for a, b in ts) / 1e3 / len(ts)
+    timed = LaunchTimer(s, args.steps, args.warmup)
 
     table = []
     for K, nbytes in C.cfg5_points():
@@ -1052,6 +1164,8 @@ def main(argv=None):
         return run_pipeline_bench(args)
     if args.workload == "sweep":
         return run_sweep_bench(args)
+    if args.workload == "configs":
+        return run_configs_bench(args)
     import torch
     rank, world, local_rank = dist_env()
     if world > 1:

@@ -192,41 +192,52 @@ __global__ void __launch_bounds__(kThreads) ar_scalar(const __grid_constant__ Ar
     }
 }
 
-// 32-byte kernels are specialised for the configured K; other K (and the
-// 16-byte fallback) use the run-time-K form.
+// The vector kernels are specialised for the configured K (both access
+// widths: 16-byte accesses serve chunks whose length is a multiple of 8 but
+// not 16, such as 25,000,000 / 8); other K use the run-time-K form.
+template <int M, int MODE, int W>
+const void* rs_vec_for(int K) {
+    switch (K) {
+        case 2: return reinterpret_cast<const void*>(rs_vec<2, M, MODE, W>);
+        case 4: return reinterpret_cast<const void*>(rs_vec<4, M, MODE, W>);
+        case 8: return reinterpret_cast<const void*>(rs_vec<8, M, MODE, W>);
+        case 16: return reinterpret_cast<const void*>(rs_vec<16, M, MODE, W>);
+        case 32: return reinterpret_cast<const void*>(rs_vec<32, M, MODE, W>);
+        case 64: return reinterpret_cast<const void*>(rs_vec<64, M, MODE, W>);
+        default: return reinterpret_cast<const void*>(rs_vec<0, M, MODE, W>);
+    }
+}
+
 template <int M, int MODE>
 const void* rs_kernel_for(int K, int W) {
-    if (W == 4) return reinterpret_cast<const void*>(rs_vec<0, M, MODE, 4>);
-    switch (K) {
-        case 2: return reinterpret_cast<const void*>(rs_vec<2, M, MODE, 8>);
-        case 4: return reinterpret_cast<const void*>(rs_vec<4, M, MODE, 8>);
-        case 8: return reinterpret_cast<const void*>(rs_vec<8, M, MODE, 8>);
-        case 16: return reinterpret_cast<const void*>(rs_vec<16, M, MODE, 8>);
-        case 32: return reinterpret_cast<const void*>(rs_vec<32, M, MODE, 8>);
-        case 64: return reinterpret_cast<const void*>(rs_vec<64, M, MODE, 8>);
-        default: return reinterpret_cast<const void*>(rs_vec<0, M, MODE, 8>);
-    }
+    return (W == 4) ? rs_vec_for<M, MODE, 4>(K) : rs_vec_for<M, MODE, 8>(K);
 }
 
 template <int M, int MODE>
 const void* rs_bf16_kernel_for(int K, int W) {
-    if (W == 4) return reinterpret_cast<const void*>(rs_bf16_vec<0, M, MODE, 4>);
-    if (K == 8) return reinterpret_cast<const void*>(rs_bf16_vec<8, M, MODE, 8>);
-    return reinterpret_cast<const void*>(rs_bf16_vec<0, M, MODE, 8>);
+    if (W == 4)
+        return (K == 8) ? reinterpret_cast<const void*>(rs_bf16_vec<8, M, MODE, 4>)
+                        : reinterpret_cast<const void*>(rs_bf16_vec<0, M, MODE, 4>);
+    return (K == 8) ? reinterpret_cast<const void*>(rs_bf16_vec<8, M, MODE, 8>)
+                    : reinterpret_cast<const void*>(rs_bf16_vec<0, M, MODE, 8>);
+}
+
+template <int MODE, int W>
+const void* ar_vec_for(int K) {
+    switch (K) {
+        case 2: return reinterpret_cast<const void*>(ar_vec<2, MODE, W>);
+        case 4: return reinterpret_cast<const void*>(ar_vec<4, MODE, W>);
+        case 8: return reinterpret_cast<const void*>(ar_vec<8, MODE, W>);
+        case 16: return reinterpret_cast<const void*>(ar_vec<16, MODE, W>);
+        case 32: return reinterpret_cast<const void*>(ar_vec<32, MODE, W>);
+        case 64: return reinterpret_cast<const void*>(ar_vec<64, MODE, W>);
+        default: return reinterpret_cast<const void*>(ar_vec<0, MODE, W>);
+    }
 }
 
 template <int MODE>
 const void* ar_kernel_for(int K, int W) {
-    if (W == 4) return reinterpret_cast<const void*>(ar_vec<0, MODE, 4>);
-    switch (K) {
-        case 2: return reinterpret_cast<const void*>(ar_vec<2, MODE, 8>);
-        case 4: return reinterpret_cast<const void*>(ar_vec<4, MODE, 8>);
-        case 8: return reinterpret_cast<const void*>(ar_vec<8, MODE, 8>);
-        case 16: return reinterpret_cast<const void*>(ar_vec<16, MODE, 8>);
-        case 32: return reinterpret_cast<const void*>(ar_vec<32, MODE, 8>);
-        case 64: return reinterpret_cast<const void*>(ar_vec<64, MODE, 8>);
-        default: return reinterpret_cast<const void*>(ar_vec<0, MODE, 8>);
-    }
+    return (W == 4) ? ar_vec_for<MODE, 4>(K) : ar_vec_for<MODE, 8>(K);
 }
 
 }  // namespace
