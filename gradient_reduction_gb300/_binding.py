@@ -120,9 +120,15 @@ def _stream(stream) -> int:
 def _need(ts: Sequence[torch.Tensor], count: int, dtype, n: int, what: str):
     if len(ts) != count:
         raise ValueError(f"{what}: expected {count} tensors, got {len(ts)}")
+    dev = None
     for t in ts:
         if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
             raise ValueError(f"{what}: need contiguous CUDA {dtype} tensors")
+        if dev is None:
+            dev = torch.cuda.current_device()
+        if t.device.index != dev:
+            # the kernels run on the current device and would fault on another's memory
+            raise ValueError(f"{what}: tensor on cuda:{t.device.index}, current device is cuda:{dev}")
         if t.numel() < n:
             raise ValueError(f"{what}: tensor of {t.numel()} elements, need {n}")
 
@@ -223,8 +229,7 @@ def dpr_flatten_plan_create(srcs: Sequence[Sequence[torch.Tensor]], numel: Seque
             raise ValueError("every rank needs P gradients")
         for p in range(P):
             t = srcs[r][p]
-            if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
-                raise ValueError("gradients must be contiguous CUDA bf16 tensors")
+            _need([t], 1, torch.bfloat16, 0, "gradients")
             if t.numel() != numel[p]:
                 raise ValueError(f"gradient {p} of rank {r}: {t.numel()} elements, numel says {numel[p]}")
             flat.append(t)
@@ -285,8 +290,7 @@ def dpr_coalesced_plan_create(tensors: Sequence[Sequence[torch.Tensor]], numel: 
             raise ValueError("every rank needs P tensors")
         for p in range(P):
             t = tensors[r][p]
-            if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
-                raise ValueError("tensors must be contiguous CUDA bf16 tensors")
+            _need([t], 1, torch.bfloat16, 0, "tensors")
             if t.numel() != numel[p]:
                 raise ValueError(f"tensor {p} of rank {r}: {t.numel()} elements, numel says {numel[p]}")
             flat.append(t)
@@ -393,8 +397,7 @@ def dpr_flatten_bucket_noalloc(srcs: Sequence[Sequence[torch.Tensor]], numel: Se
             raise ValueError("every rank needs P gradients")
         for p in range(P):
             t = srcs[r][p]
-            if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
-                raise ValueError("gradients must be contiguous CUDA bf16 tensors")
+            _need([t], 1, torch.bfloat16, 0, "gradients")
             if t.numel() != numel[p]:
                 raise ValueError(f"gradient {p} of rank {r}: {t.numel()} elements, numel says {numel[p]}")
             flat.append(t)

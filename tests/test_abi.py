@@ -218,3 +218,20 @@ def test_coalesced_plan_refuses_more_tiles_than_a_grid_holds(L):
     h = ctypes.c_void_p()
     assert L.dpr_coalesced_plan_create(ctypes.byref(h), K, P, t, numel, None) == UNSUP
     assert h.value is None
+
+
+def test_binding_refuses_host_tensors_before_touching_the_library():
+    """The Python binding checks tensors first: host (CPU) tensors, wrong
+    dtypes and short tensors are refused with ValueError, with no CUDA call."""
+    import torch
+    import gradient_reduction_gb300 as dpr
+    x = [torch.zeros(64, dtype=torch.bfloat16) for _ in range(4)]
+    out = [torch.zeros(16, dtype=torch.float32) for _ in range(4)]
+    for call in (lambda: dpr.dpr_reduce_scatter(x, 4, 1, 64, out),
+                 lambda: dpr.dpr_allgather([t[:16] for t in x], 4, 64, x),
+                 lambda: dpr.dpr_allreduce(x, 4, 64, x),
+                 lambda: dpr.dpr_cast_bf16_to_fp32(x[0], out[0]),
+                 lambda: dpr.dpr_flatten_plan_create([[t] for t in x], [64], [0], 64),
+                 lambda: dpr.dpr_coalesced_plan_create([[t] for t in x], [64])):
+        with pytest.raises(ValueError):
+            call()
