@@ -149,9 +149,9 @@ dpr_status dpr_allreduce(const void* const* in, int K, int64_t N, void* const* o
  * gradients already exist as separate buffers, so flattening is a copy.
  *
  * dpr_flatten_plan_create records the table once (offsets are fixed after
- * initialisation): it allocates a device copy of it (the only allocation in
- * this library), uploads it on `stream` and waits for the upload, so the plan
- * can then be used on any stream.
+ * initialisation): it allocates a device copy of it (plan and pipeline
+ * constructors are the only calls that allocate), uploads it on `stream` and
+ * waits for the upload, so the plan can then be used on any stream.
  *   src          host array [K*P]; src[r*P + p] = rank r's gradient p, bf16.
  *   numel, offset host arrays [P], elements; spans must lie inside
  *                [0, bucket_numel) and not overlap.  numel[p] == 0 is allowed.
