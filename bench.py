@@ -136,6 +136,29 @@ def max_over_ranks(x: float, device=None) -> float:
     return float(t.item())
 
 
+def all_ranks(flag: bool, device=None) -> bool:
+    """True only if flag is true on every rank (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return flag
+    t = torch.tensor([1 if flag else 0], dtype=torch.int32, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return bool(t.item())
+
+
+def host_available_bytes() -> int:
+    """MemAvailable of this host (Linux), or a very large number elsewhere."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 1 << 62
+
+
 def barrier(device=None):
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
@@ -875,12 +898,29 @@ def run_e2e(wl, args, step_bytes):
     step still moves all of its own bytes inside the timed region."""
     import torch
     dev = wl.dev
+    _, world, _ = dist_env()
+    pinned = sum(t.numel() * t.element_size() for t in wl.inputs() + wl.outputs())
+    local = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+    # every rank of this host pins its own copy: all ranks run the e2e steps,
+    # or none does (they meet in a collective at the end)
+    fits = host_available_bytes() >= local * pinned * 1.1 + (8 << 30)
+    h_in = h_out = None
+    if fits:
+        try:
+            h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl.inputs()]
+            h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl.outputs()]
+        except RuntimeError:
+            fits = False
+    if not all_ranks(fits, dev):
+        h_in = h_out = None
+        torch.cuda.empty_cache()
+        return {"value": None, "unit": UNIT,
+                "skipped": f"{local} rank(s) on this host need {local * pinned / 1e9:.0f} GB of "
+                           "pinned host memory for the step's inputs and results"}
     # two buffer sets (a third one measured no faster on GB300: the host link,
     # not the set reuse, bounds the step)
     nsets = 2
     sets = [wl] + [Workload(dev, wl.stream, args.n_per_rank, fill=False) for _ in range(nsets - 1)]
-    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl.inputs()]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl.outputs()]
     for h, d in zip(h_in, wl.inputs()):
         h.copy_(d)
     torch.cuda.synchronize()
@@ -933,7 +973,6 @@ def run_e2e(wl, args, step_bytes):
     torch.cuda.synchronize()
     el = t0.elapsed_time(t1) / 1e3
     el = max_over_ranks(el, dev)
-    _, world, _ = dist_env()
     for w in sets[1:]:
         w.plan.close()
     for w in sets:

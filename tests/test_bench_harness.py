@@ -31,9 +31,10 @@ def _worker(rank, world, port, q):
     elapsed = 1.0 + rank          # rank 1 is the slow one
     mx = bench.max_over_ranks(elapsed)
     val = bench.job_value(1e9, 10, w, mx)
+    agree = (bench.all_ranks(True), bench.all_ranks(rank == 0))   # one rank says no
     bench.barrier()
     dist.destroy_process_group()
-    q.put((r, w, lr, mx, val))
+    q.put((r, w, lr, mx, val, agree))
 
 
 def test_two_rank_harness_gloo():
@@ -48,9 +49,10 @@ def test_two_rank_harness_gloo():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert [x[:3] for x in res] == [(0, 2, 0), (1, 2, 1)]
-    for _, _, _, mx, val in res:
+    for _, _, _, mx, val, agree in res:
         assert mx == 2.0                     # the slowest rank's time
         assert val == pytest.approx(1e9 * 10 * 2 / 2.0 / 1e9)
+        assert agree == (True, False)        # every rank sees the same decision
 
 
 def _dying_worker(rank, world, port, q):
@@ -95,6 +97,8 @@ def test_job_value_single():
     import bench
     assert bench.job_value(2e9, 5, 1, 1.0) == pytest.approx(10.0)
     assert bench.max_over_ranks(3.5) == 3.5      # no process group: identity
+    assert bench.all_ranks(False) is False and bench.all_ranks(True) is True
+    assert bench.host_available_bytes() > 0
 
 
 def test_reference_arm_line():
