@@ -75,6 +75,35 @@ def test_parity_against_overlap_off_and_oracle(policy, n_buffers):
         p.close()
 
 
+@pytest.mark.parametrize("max_blocks", [0, 24])
+def test_hop_mode_accumulate_and_block_budget(max_blocks):
+    """Per-hop bf16 sums accumulated into existing partitions, with the
+    reductions unbounded or held to a small block budget (grid-stride):
+    bit-exact against the oracle."""
+    dev = H.device()
+    cfg, numel, buckets, grads, plans = _small_model(dev)
+    K = cfg.K
+    init = [[syn.gauss_bf16(0, b.numel // K, syn.stream_key(77, bi, 0, j), 1e-2).float()
+             for j in range(K)] for bi, b in enumerate(buckets)]
+    outs = [[t.clone().to(dev) for t in row] for row in init]
+    cur = torch.cuda.Stream()
+    with dpr.BucketPipeline(K, max(b.numel for b in buckets), 2, dpr.WAIT_PER_BUFFER,
+                            max_blocks=max_blocks) as pipe:
+        for plan, o in zip(plans, outs):
+            pipe.submit(plan, o, mode=ring.HOP_BF16, scale=1.0 / K, accumulate=True, stream=cur)
+        pipe.flush(stream=cur)
+        cur.synchronize()
+    for bi, b in enumerate(buckets):
+        flat = ofl.flatten_bucket([[H.bits(grads[r][p]) for p in b.params] for r in range(K)],
+                                  [numel[p] for p in b.params], b.offsets, b.numel)
+        want, _ = ring.reduce_scatter(flat, K, 1, ring.HOP_BF16, 1.0 / K,
+                                      out_init=[t.numpy() for t in init[bi]])
+        for j in range(K):
+            H.assert_f32_equal(outs[bi][j].cpu().numpy(), want[j], f"bucket {bi} shard {j}")
+    for p in plans:
+        p.close()
+
+
 def test_rapid_reuse_of_both_buffers():
     """The producer rewrites the same gradient tensors for every bucket on the
     compute stream; 48 buckets go through 2 physical buffers back to back."""
