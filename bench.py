@@ -690,6 +690,29 @@ def run_configs_bench(args):
         row(3, "flatten+rs_fp32 per bucket", nbytes, t, launches=2 * len(steps))
         for plan, *_ in steps:
             plan.close()
+        # the same reduction straight from the fragments: no bucket is written or re-read
+        fused = []
+        for b, nb in enumerate(bucket_numel):
+            ps = [p for p in range(len(numel)) if bucket_of[p] == b]
+            fplan = dpr.dpr_fragments_plan_create([[grads[r][p] for p in ps] for r in range(K)],
+                                                  [numel[p] for p in ps], [offset[p] for p in ps],
+                                                  nb, stream=s)
+            fused.append(fplan)
+        outs_by_bucket = []
+        at = 0
+        for nb in bucket_numel:
+            outs_by_bucket.append([part[j, at:at + nb // K] for j in range(K)])
+            at += nb // K
+
+        def backward_fused():
+            for fplan, outs in zip(fused, outs_by_bucket):
+                dpr.dpr_reduce_scatter_fragments(fplan, outs, mode=dpr.RING_FP32, stream=s)
+
+        fbytes = 2 * K * sum(numel) + 4 * total
+        t_f = timed(backward_fused, fbytes)
+        row(3, "rs_fp32 from fragments per bucket", fbytes, t_f, launches=len(fused))
+        for fplan in fused:
+            fplan.close()
         del steps, grads, part, ipg
         torch.cuda.empty_cache()
         # configuration 4

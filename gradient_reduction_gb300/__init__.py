@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     RING_FP32,
     DprError,
     FlattenPlan,
+    FragmentsPlan,
     dpr_allgather,
     dpr_allreduce,
     dpr_allgather_coalesced,
@@ -32,9 +33,12 @@ from ._binding import (  # noqa: F401
     dpr_flatten_bucket_noalloc,
     dpr_flatten_plan_create,
     dpr_flatten_plan_destroy,
+    dpr_fragments_plan_create,
+    dpr_fragments_plan_destroy,
     dpr_reduce_scatter,
     dpr_reduce_scatter_bf16,
     dpr_reduce_scatter_coalesced,
+    dpr_reduce_scatter_fragments,
     dpr_strerror,
     dpr_version,
     lib,

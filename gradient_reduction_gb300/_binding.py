@@ -41,6 +41,10 @@ _SIGS = {
                           ctypes.POINTER(ctypes.c_int)],
     "dpr_flatten_bucket_noalloc": [ctypes.c_int, ctypes.c_int, _pp, _i64p, _i64p, ctypes.c_int64,
                                    _pp, _c_p],
+    "dpr_fragments_plan_create": [ctypes.POINTER(_c_p), ctypes.c_int, ctypes.c_int, _pp, _i64p,
+                                  _i64p, ctypes.c_int64, _c_p],
+    "dpr_reduce_scatter_fragments": [_c_p, _pp, ctypes.c_int, ctypes.c_float, ctypes.c_int, _c_p],
+    "dpr_fragments_plan_destroy": [_c_p],
     "dpr_coalesced_plan_create": [ctypes.POINTER(_c_p), ctypes.c_int, ctypes.c_int, _pp, _i64p,
                                   _c_p],
     "dpr_coalesced_partition_numel": [_c_p, _i64p],
@@ -249,6 +253,61 @@ def dpr_flatten_bucket(plan: FlattenPlan, dst: Sequence[torch.Tensor], stream=No
 
 
 def dpr_flatten_plan_destroy(plan: FlattenPlan) -> None:
+    plan.close()
+
+
+class FragmentsPlan(FlattenPlan):
+    """Owns a dpr_fragments_plan and keeps its source gradients alive."""
+
+    def close(self):
+        if self.handle:
+            h, self.handle = self.handle, None
+            _check("dpr_fragments_plan_destroy", lib().dpr_fragments_plan_destroy(h))
+
+
+def _grad_table(srcs: Sequence[Sequence[torch.Tensor]], numel: Sequence[int]) -> list:
+    K, P = len(srcs), len(numel)
+    flat = []
+    for r in range(K):
+        if len(srcs[r]) != P:
+            raise ValueError("every rank needs P gradients")
+        for p in range(P):
+            t = srcs[r][p]
+            _need([t], 1, torch.bfloat16, 0, "gradients")
+            if t.numel() != numel[p]:
+                raise ValueError(f"gradient {p} of rank {r}: {t.numel()} elements, numel says {numel[p]}")
+            flat.append(t)
+    return flat
+
+
+def dpr_fragments_plan_create(srcs: Sequence[Sequence[torch.Tensor]], numel: Sequence[int],
+                              offset: Sequence[int], bucket_numel: int,
+                              stream=None) -> FragmentsPlan:
+    """srcs[r][p]: rank r's gradient p (bf16, numel[p] elements); the bucket
+    layout as for dpr_flatten_plan_create."""
+    K, P = len(srcs), len(numel)
+    flat = _grad_table(srcs, numel)
+    h = ctypes.c_void_p()
+    n_arr = (ctypes.c_int64 * max(P, 1))(*numel)
+    o_arr = (ctypes.c_int64 * max(P, 1))(*offset)
+    st = lib().dpr_fragments_plan_create(ctypes.byref(h), K, P, _ptrs(flat), n_arr, o_arr,
+                                         bucket_numel, _stream(stream))
+    _check("dpr_fragments_plan_create", st)
+    return FragmentsPlan(h.value, K, bucket_numel, flat)
+
+
+def dpr_reduce_scatter_fragments(plan: FragmentsPlan, outputs: Sequence[torch.Tensor],
+                                 mode=RING_FP32, scale: float | None = None,
+                                 accumulate: bool = False, stream=None) -> None:
+    """outputs[j]: fp32 shard j of the bucket (bucket_numel / K,)."""
+    _need(outputs, plan.K, torch.float32, plan.bucket_numel // plan.K, "outputs")
+    st = lib().dpr_reduce_scatter_fragments(plan.handle, _ptrs(outputs), _MODES[mode],
+                                            1.0 / plan.K if scale is None else scale,
+                                            int(bool(accumulate)), _stream(stream))
+    _check("dpr_reduce_scatter_fragments", st)
+
+
+def dpr_fragments_plan_destroy(plan: FragmentsPlan) -> None:
     plan.close()
 
 

@@ -212,6 +212,39 @@ dpr_status dpr_flatten_bucket_noalloc(int K, int P, const void* const* src, cons
                                       void* const* dst, void* stream);
 
 /*
+ * Reduce-scatter of a flat bucket straight from its fragments: the result of
+ * dpr_flatten_bucket followed by dpr_reduce_scatter (M = 1), without the flat
+ * bucket.  In ZeRO the gradients are written into the IPG bucket in the first
+ * place (DeepSpeed ZeRO-3 source walkthrough, sections 3.2 and 5.1); when
+ * they already exist as separate buffers, gathering them costs a write and a
+ * re-read of the whole bucket, which this call skips.
+ *
+ * dpr_fragments_plan_create takes the arguments of dpr_flatten_plan_create
+ * (same meanings and checks) and additionally needs K >= 2 and
+ * bucket_numel % K == 0.  It records, for every tile of every chunk, which
+ * gradient (or gap) covers which run of its elements, allocates and uploads
+ * those tables and the pointer table (cudaMalloc), and waits for the upload.
+ *
+ * dpr_reduce_scatter_fragments: with B_r = rank r's bucket as
+ * dpr_flatten_bucket would lay it out and positions no gradient covers equal
+ * to zero,
+ *     out[j][t] = scale * (ring-order sum over ranks, starting at rank j, of
+ *                 B_r[j*S + t])                                   (copy_)
+ *     out[j][t] = out[j][t] + that                                 (add_)
+ * S = bucket_numel / K; mode, scale and accumulate as in dpr_reduce_scatter.
+ * out: host array [K] of fp32 shards of S elements, not overlapping each other
+ * or any source gradient.  One kernel launch on `stream`.
+ */
+typedef struct dpr_fragments_plan dpr_fragments_plan;
+
+dpr_status dpr_fragments_plan_create(dpr_fragments_plan** plan, int K, int P, const void* const* src,
+                                     const int64_t* numel, const int64_t* offset,
+                                     int64_t bucket_numel, void* stream);
+dpr_status dpr_reduce_scatter_fragments(const dpr_fragments_plan* plan, float* const* out, int mode,
+                                        float scale, int accumulate, void* stream);
+dpr_status dpr_fragments_plan_destroy(dpr_fragments_plan* plan);
+
+/*
  * Per-parameter partitioning (ZeRO-3): the discrete reduction path and the
  * parameter all-gather.  DeepSpeed ZeRO-3 source walkthrough, section 1:
  * every parameter lives as a 1/N shard per rank; section 5.2: with

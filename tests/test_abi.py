@@ -35,7 +35,7 @@ def _declared():
 
 def test_exports_every_declared_function(L):
     names = _declared()
-    assert len(names) == 28
+    assert len(names) == 31
     for n in names:
         assert hasattr(L, n), n
 
@@ -235,3 +235,25 @@ def test_binding_refuses_host_tensors_before_touching_the_library():
                  lambda: dpr.dpr_coalesced_plan_create([[t] for t in x], [64])):
         with pytest.raises(ValueError):
             call()
+
+
+def test_fragments_plan_rejections(L):
+    """Host-side checks of the fused gather + reduce-scatter plan; the fake
+    addresses are never dereferenced (every case is refused before any CUDA
+    call)."""
+    h = ctypes.c_void_p()
+    c = L.dpr_fragments_plan_create
+    K, P = 2, 2
+    src = _arr([BASE, BASE + (1 << 20), BASE + (2 << 20), BASE + (3 << 20)])
+    n = (ctypes.c_int64 * P)(16, 16)
+    off = (ctypes.c_int64 * P)(0, 16)
+    assert c(ctypes.byref(h), 1, P, src, n, off, 32, None) == INVALID          # K < 2
+    assert c(ctypes.byref(h), K, P, src, n, off, 33, None) == INVALID          # bucket % K
+    assert c(ctypes.byref(h), K, P, src, n, off, 24, None) == INVALID          # span past the bucket
+    assert c(ctypes.byref(h), K, P, src, n, (ctypes.c_int64 * P)(0, 8), 32, None) == ALIAS
+    odd = _arr([BASE + 1, BASE + (1 << 20), BASE + (2 << 20), BASE + (3 << 20)])
+    assert c(ctypes.byref(h), K, P, odd, n, off, 32, None) == ALIGN
+    assert c(ctypes.byref(h), K, P, src, n, off, 1 << 40, None) == UNSUP
+    assert h.value is None
+    assert L.dpr_reduce_scatter_fragments(None, None, 0, 1.0, 0, None) == INVALID
+    assert L.dpr_fragments_plan_destroy(None) == OK
