@@ -711,6 +711,18 @@ def run_configs_bench(args):
         fbytes = 2 * K * sum(numel) + 4 * total
         t_f = timed(backward_fused, fbytes)
         row(3, "rs_fp32 from fragments per bucket", fbytes, t_f, launches=len(fused))
+        # the 42 launches captured once in a CUDA graph and replayed
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            backward_fused()
+        def replay():
+            with torch.cuda.stream(s):
+                graph.replay()
+
+        t_g = timed(replay, fbytes)
+        row(3, "rs_fp32 from fragments per bucket, CUDA graph", fbytes, t_g, launches=len(fused))
+        del graph
         for fplan in fused:
             fplan.close()
         del steps, grads, part, ipg
