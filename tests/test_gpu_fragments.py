@@ -20,7 +20,7 @@ import gradient_reduction_gb300 as dpr
 from oracle import flatten as ofl
 from oracle import ring
 from tests import gpu_helpers as H
-from tests.test_gpu_guards import Arena
+from tests.gpu_helpers import Arena
 from workloads import configs as C
 from workloads import synthetic as syn
 

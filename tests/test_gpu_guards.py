@@ -19,48 +19,10 @@ from oracle import bf16 as obf
 from oracle import flatten as ofl
 from oracle import ring
 from tests import gpu_helpers as H
+from tests.gpu_helpers import PAT, Arena
 from workloads import synthetic as syn
 
 pytestmark = pytest.mark.gpu
-
-PAT = 0xA5
-GAP = 768
-
-
-class Arena:
-    """Buffers carved out of one uint8 device allocation filled with PAT."""
-
-    def __init__(self):
-        self.specs = []       # (byte offset, element count, dtype)
-        self.size = GAP
-
-    def add(self, n: int, dtype, shift: int = 0) -> int:
-        off = (self.size + GAP + 255) // 256 * 256 + shift
-        self.specs.append((off, n, dtype))
-        self.size = off + n * torch.tensor([], dtype=dtype).element_size()
-        return len(self.specs) - 1
-
-    def build(self, dev):
-        self.buf = torch.full((self.size + GAP,), PAT, dtype=torch.uint8, device=dev)
-        self.views = [self.buf[off:off + n * torch.tensor([], dtype=dt).element_size()].view(dt)
-                      for off, n, dt in self.specs]
-        return self.views
-
-    def snapshot(self):
-        torch.cuda.synchronize()
-        self.before = self.buf.cpu().numpy().copy()
-
-    def check_untouched(self, written):
-        """written: list of (buffer index, first element, element count)."""
-        torch.cuda.synchronize()
-        after = self.buf.cpu().numpy()
-        free = np.ones(after.size, bool)
-        for i, e0, n in written:
-            off, _, dt = self.specs[i]
-            es = torch.tensor([], dtype=dt).element_size()
-            free[off + e0 * es: off + (e0 + n) * es] = False
-        bad = np.flatnonzero(free & (after != self.before))
-        assert bad.size == 0, f"{bad.size} bytes outside the written regions changed, first at {bad[0]}"
 
 
 def _bf16_data(n, seed):
