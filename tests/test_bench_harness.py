@@ -137,3 +137,37 @@ def test_ring_busbw_matches_the_ring_simulation_traffic(K):
     for name, elems in sent.items():
         assert bench.ring_busbw(name, K, N, t) * t * 1e9 == pytest.approx(2 * elems)
     assert bench.ring_busbw("flatten", K, N, t) is None
+
+
+class _HostOnlyWorkload:
+    """Stand-in for the bench workload with small host tensors: enough for the
+    end-to-end leg's host-memory decision, which runs before any device work."""
+
+    def __init__(self):
+        import torch
+        self.dev = torch.device("cpu")
+        self._in = [torch.zeros(1024, dtype=torch.bfloat16)]
+        self._out = [torch.zeros(256, dtype=torch.float32)]
+
+    def inputs(self):
+        return self._in
+
+    def outputs(self):
+        return self._out
+
+
+def test_e2e_is_skipped_when_host_memory_cannot_hold_it(monkeypatch):
+    """Too little available host memory, or a pinned allocation that fails,
+    makes the end-to-end leg report itself skipped instead of failing."""
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.parse_args([])
+    monkeypatch.setattr(bench, "host_available_bytes", lambda: 0)
+    e2e = bench.run_e2e(_HostOnlyWorkload(), args, 1)
+    assert e2e["value"] is None and "pinned host memory" in e2e["skipped"]
+    import torch
+    if not torch.cuda.is_available():
+        # plenty of memory, but no CUDA to pin it with: the allocation fails
+        monkeypatch.setattr(bench, "host_available_bytes", lambda: 1 << 62)
+        e2e = bench.run_e2e(_HostOnlyWorkload(), args, 1)
+        assert e2e["value"] is None
