@@ -1216,7 +1216,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage": "bf16 gradients and parameters, fp32 partitions",
         "data": "synthetic (seeded counter-hash generator)",
         "config": common_config(1),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -1258,7 +1258,7 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(res["max_elapsed"] / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded counter-hash generator)",
+        "dtype": "f32", "storage": "bf16 gradients and parameters, fp32 partitions", "data": "synthetic (seeded counter-hash generator)",
         "config": common_config(world),
         "pct_of_peak": round(100 * value / world / peak, 2),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(d["gbs"], 1),
