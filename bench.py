@@ -89,12 +89,22 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--workload", choices=["zero_bucket", "zero3_per_param", "bucket_pipeline",
-                                          "bf16_partition", "sweep", "configs"],
+                                          "bf16_partition", "sweep", "configs", "point"],
                    default="zero_bucket",
                    help="zero_bucket: the headline step (default); zero3_per_param: the ZeRO-3 "
                         "discrete path on config 3's 56 gradients; bucket_pipeline: backward "
                         "time under the stream-overlap policies; bf16_partition: reduce-scatter "
-                        "into bf16 partitions over two micro steps and the step-time cast")
+                        "into bf16 partitions over two micro steps and the step-time cast; "
+                        "sweep: configuration 5; configs: configurations 1-4; point: one "
+                        "reduce-scatter / all-gather / all-reduce point chosen by --K, "
+                        "--bytes-per-rank, --mode, --micro, --seed")
+    p.add_argument("--K", type=int, default=8, help="point: simulated ranks")
+    p.add_argument("--bytes-per-rank", type=int, default=1 << 28, help="point: bf16 bytes per rank")
+    p.add_argument("--mode", choices=["ring_fp32", "hop_bf16"], default="ring_fp32",
+                   help="point: reduce-scatter summation mode")
+    p.add_argument("--micro", type=int, default=1, choices=[1, 2],
+                   help="point: micro-batches accumulated before the reduce")
+    p.add_argument("--seed", type=int, default=0, help="point: generator seed")
     p.add_argument("--only", choices=STEP_KERNELS + Z3_KERNELS + BF16_KERNELS, default=None,
                    help="profile helper: launch only this kernel per step")
     p.add_argument("--graph", action="store_true",
@@ -747,6 +757,54 @@ def run_configs_bench(args):
     return 0
 
 
+def run_point_bench(args):
+    """One point chosen on the command line: the reduce-scatter (--mode,
+    --micro), all-gather and all-reduce at --K ranks and --bytes-per-rank,
+    seeded gradients ~N(0, 1e-3), timed like the sweep."""
+    import torch
+    import gradient_reduction_gb300 as dpr
+    from workloads import synthetic as syn
+    K, M = args.K, args.micro
+    N = args.bytes_per_rank // 2
+    if N <= 0 or N % K:
+        raise SystemExit("--bytes-per-rank / 2 must be a positive multiple of --K")
+    S = N // K
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = torch.cuda.Stream(device=dev)
+    timed = LaunchTimer(s, args.steps, args.warmup)
+    mode = dpr.RING_FP32 if args.mode == "ring_fp32" else dpr.HOP_BF16
+    with torch.cuda.stream(s):
+        x = torch.empty(M * K, N, dtype=torch.bfloat16, device=dev)
+        for i in range(M * K):
+            syn.gauss_bf16(0, N, syn.stream_key(args.seed, i % K, i // K), 1e-3, device=dev,
+                           out=x[i])
+        xs = list(x.unbind(0))
+        out = list(torch.empty(K, S, dtype=torch.float32, device=dev).unbind(0))
+        rows = {}
+        b_rs = 2 * M * K * N + 4 * N
+        t = timed(lambda: dpr.dpr_reduce_scatter(xs, K, M, N, out, mode=mode, stream=s), b_rs)
+        rows["reduce_scatter"] = {"bytes": b_rs, "us": round(t * 1e6, 2), "gbs": round(b_rs / t / 1e9, 1)}
+        del out
+        y = list(torch.empty(K, N, dtype=torch.bfloat16, device=dev).unbind(0))
+        b_ag = 2 * N + 2 * K * N
+        shards = [xs[j][:S] for j in range(K)]
+        t = timed(lambda: dpr.dpr_allgather(shards, K, N, y, stream=s), b_ag)
+        rows["allgather"] = {"bytes": b_ag, "us": round(t * 1e6, 2), "gbs": round(b_ag / t / 1e9, 1)}
+        b_ar = 4 * K * N
+        t = timed(lambda: dpr.dpr_allreduce(xs[:K], K, N, y, mode=mode, stream=s), b_ar)
+        rows["allreduce"] = {"bytes": b_ar, "us": round(t * 1e6, 2), "gbs": round(b_ar / t / 1e9, 1)}
+    peak, kind = load_peaks()
+    line = {"metric": METRIC, "value": rows["reduce_scatter"]["gbs"], "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "config": {"workload": "point", "K": K, "bytes_per_rank": args.bytes_per_rank,
+                       "mode": args.mode, "micro_batches": M, "seed": args.seed},
+            "value_is": "the reduce-scatter's GB/s", "peak": peak, "peak_kind": kind,
+            "ops": rows}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_sweep_bench(args):
     """Configuration 5's sweep: effective GB/s of the reduce-scatter (both
     modes, 2 micro-batches), all-gather and all-reduce for K in
@@ -1240,6 +1298,8 @@ def main(argv=None):
         return run_sweep_bench(args)
     if args.workload == "configs":
         return run_configs_bench(args)
+    if args.workload == "point":
+        return run_point_bench(args)
     import torch
     rank, world, local_rank = dist_env()
     if world > 1:
