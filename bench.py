@@ -59,18 +59,18 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum at the bench's full size
     # (K=8, N=2**29), one launch each (profiles/step_k8_1GiB_dram_traffic.md); src_sha is
     # kernel_src_sha(kernel) of the sources the capture was taken from
-    "flatten": {"bytes": 17_129_000_000, "src_sha": "81b7d453ae3c43eb"},
-    "rs_fp32_m2": {"bytes": 19_312_000_000, "src_sha": "f0c947c43bd74401"},
-    "rs_hop_m2_acc": {"bytes": 21_459_000_000, "src_sha": "f0c947c43bd74401"},
-    "allgather": {"bytes": 9_600_000_000, "src_sha": "81b7d453ae3c43eb"},
-    "allreduce": {"bytes": 17_122_000_000, "src_sha": "f0c947c43bd74401"},
+    "flatten": {"bytes": 17_129_000_000, "src_sha": "37b74f39084a227f"},
+    "rs_fp32_m2": {"bytes": 19_312_000_000, "src_sha": "7aab38c883045de4"},
+    "rs_hop_m2_acc": {"bytes": 21_460_000_000, "src_sha": "7aab38c883045de4"},
+    "allgather": {"bytes": 9_600_000_000, "src_sha": "37b74f39084a227f"},
+    "allreduce": {"bytes": 17_121_000_000, "src_sha": "7aab38c883045de4"},
     # the same metrics on the other workloads' first timed step
     # (profiles/zero3_and_bf16_partition_dram_traffic.md)
-    "rs_coalesced": {"bytes": 22_004_000_000, "src_sha": "a947686bcfd68570"},
-    "ag_coalesced": {"bytes": 19_755_000_000, "src_sha": "89f935c89cda9999"},
-    "rs_bf16_copy": {"bytes": 9_654_000_000, "src_sha": "f0c947c43bd74401"},
-    "rs_bf16_add": {"bytes": 10_725_000_000, "src_sha": "f0c947c43bd74401"},
-    "cast": {"bytes": 3_163_000_000, "src_sha": "b5d5cff3cb193264"},
+    "rs_coalesced": {"bytes": 22_005_000_000, "src_sha": "410864765ad8f3d1"},
+    "ag_coalesced": {"bytes": 19_756_000_000, "src_sha": "ba2c21a57ae06ff6"},
+    "rs_bf16_copy": {"bytes": 9_654_000_000, "src_sha": "7aab38c883045de4"},
+    "rs_bf16_add": {"bytes": 10_725_000_000, "src_sha": "7aab38c883045de4"},
+    "cast": {"bytes": 3_163_000_000, "src_sha": "70432212ab8c1e1f"},
 }
 
 
@@ -209,15 +209,16 @@ def load_peaks():
 
 # Source files that determine each timed kernel and its launch (kernel code,
 # shared device headers, host-side layout selection and grid sizing).
-_COMMON_SRC = ["dpr_device.cuh", "dpr_kernels.h", "dpr_api.cu"]
+_COMMON_SRC = ["dpr_device.cuh", "dpr_kernels.h", "dpr_api.cu", "host_checks.h"]
 KERNEL_SOURCES = {
     "flatten": ["gather_kernels.cu"] + _COMMON_SRC,
     "allgather": ["gather_kernels.cu"] + _COMMON_SRC,
     "rs_fp32_m2": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
     "rs_hop_m2_acc": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
     "allreduce": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
-    "rs_coalesced": ["coalesced.cu", "dpr_ring.cuh", "dpr_device.cuh", "dpr_kernels.h"],
-    "ag_coalesced": ["coalesced.cu", "dpr_device.cuh", "dpr_kernels.h"],
+    "rs_coalesced": ["coalesced.cu", "dpr_ring.cuh", "dpr_device.cuh", "dpr_kernels.h",
+                     "host_checks.h"],
+    "ag_coalesced": ["coalesced.cu", "dpr_device.cuh", "dpr_kernels.h", "host_checks.h"],
     "rs_bf16_copy": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
     "rs_bf16_add": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
     "cast": ["reduce_kernels.cu"] + _COMMON_SRC,

@@ -24,6 +24,7 @@
 #include "dpr_device.cuh"
 #include "dpr_kernels.h"
 #include "dpr_ring.cuh"
+#include "host_checks.h"
 
 namespace dpr {
 namespace {
@@ -134,10 +135,6 @@ __global__ void __launch_bounds__(kThreads) ag_coalesced(const __grid_constant__
     for (int64_t i = threadIdx.x; i < n; i += kThreads) dst[i] = src[i];
 }
 
-struct Span {
-    uintptr_t lo, hi;
-};
-
 template <int MODE>
 const void* rs_coalesced_for(int K) {
     switch (K) {
@@ -150,10 +147,6 @@ const void* rs_coalesced_for(int K) {
         default: return reinterpret_cast<const void*>(rs_coalesced<0, MODE>);
     }
 }
-
-bool overlap(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; }
-
-bool aligned_to(const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; }
 
 dpr_status coal_cuda(cudaError_t e) { return record_cuda_status(e); }
 
@@ -188,14 +181,6 @@ void free_plan(dpr_coalesced_plan* pl) {
     delete pl;
 }
 
-template <typename T>
-cudaError_t upload(T** dst, const std::vector<T>& src, cudaStream_t st) {
-    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), src.size() * sizeof(T));
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice, st);
-    return e;
-}
-
 }  // namespace
 
 extern "C" {
@@ -214,7 +199,7 @@ dpr_status dpr_coalesced_plan_create(dpr_coalesced_plan** plan, int K, int P,
             const void* t = tensors[size_t(r) * P + p];
             if (numel[p] == 0) continue;
             if (!t) return DPR_ERR_INVALID_ARG;
-            if (!aligned_to(t, 2)) return DPR_ERR_ALIGNMENT;
+            if (!aligned(t, 2)) return DPR_ERR_ALIGNMENT;
             const uintptr_t a = reinterpret_cast<uintptr_t>(t);
             spans.push_back(Span{a, a + uintptr_t(numel[p]) * 2});
         }
@@ -246,7 +231,7 @@ dpr_status dpr_coalesced_plan_create(dpr_coalesced_plan** plan, int K, int P,
             g.j = j;
             bool vec = (s % 16 == 0) && (off % 16 == 0);
             for (int r = 0; r < K && vec; ++r)
-                vec = aligned_to(static_cast<const uint16_t*>(tensors[size_t(r) * P + p]) + j * s, 32);
+                vec = aligned(static_cast<const uint16_t*>(tensors[size_t(r) * P + p]) + j * s, 32);
             g.vec = vec ? 1 : 0;
             g.pad = 0;
             tiles += (s + kCoalTile - 1) / kCoalTile;
@@ -309,17 +294,17 @@ dpr_status dpr_reduce_scatter_coalesced(const dpr_coalesced_plan* plan, float* c
     std::vector<Span> outs;
     for (int j = 0; j < K; ++j) {
         if (!out[j]) return DPR_ERR_INVALID_ARG;
-        if (!aligned_to(out[j], 4)) return DPR_ERR_ALIGNMENT;
-        a32 = a32 && aligned_to(out[j], 32);
+        if (!aligned(out[j], 4)) return DPR_ERR_ALIGNMENT;
+        a32 = a32 && aligned(out[j], 32);
         const uintptr_t a = reinterpret_cast<uintptr_t>(out[j]);
         outs.push_back(Span{a, a + uintptr_t(plan->partition_numel) * 4});
     }
     for (int j = 0; j < K; ++j)
         for (int q = j + 1; q < K; ++q)
-            if (overlap(outs[j], outs[q])) return DPR_ERR_ALIAS;
+            if (overlaps(outs[j], outs[q])) return DPR_ERR_ALIAS;
     for (const Span& t : plan->tensor_spans)
         for (const Span& o : outs)
-            if (overlap(t, o)) return DPR_ERR_ALIAS;
+            if (overlaps(t, o)) return DPR_ERR_ALIAS;
     if (plan->n_tiles == 0) return DPR_OK;
     CoalParams prm;
     std::memset(&prm, 0, sizeof(prm));
@@ -351,12 +336,12 @@ dpr_status dpr_allgather_coalesced(const dpr_coalesced_plan* plan, const void* c
     bool a32 = true;
     for (int j = 0; j < K; ++j) {
         if (!shards[j]) return DPR_ERR_INVALID_ARG;
-        if (!aligned_to(shards[j], 2)) return DPR_ERR_ALIGNMENT;
-        a32 = a32 && aligned_to(shards[j], 32);
+        if (!aligned(shards[j], 2)) return DPR_ERR_ALIGNMENT;
+        a32 = a32 && aligned(shards[j], 32);
         const uintptr_t a = reinterpret_cast<uintptr_t>(shards[j]);
         const Span sp{a, a + uintptr_t(plan->partition_numel) * 2};
         for (const Span& t : plan->tensor_spans)
-            if (overlap(t, sp)) return DPR_ERR_ALIAS;
+            if (overlaps(t, sp)) return DPR_ERR_ALIAS;
     }
     if (plan->n_tiles == 0) return DPR_OK;
     CoalParams prm;

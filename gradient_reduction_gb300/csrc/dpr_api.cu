@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "dpr_kernels.h"
+#include "host_checks.h"
 
 namespace dpr {
 namespace {
@@ -27,26 +28,6 @@ dpr_status cuda_status(cudaError_t e) {
 dpr_status record_cuda_status(cudaError_t e) { return cuda_status(e); }
 
 namespace {
-
-struct Span {
-    uintptr_t lo, hi;  // [lo, hi)
-};
-
-bool overlaps(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; }
-
-Span span_of(const void* p, uint64_t bytes) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    return Span{a, a + uintptr_t(bytes)};
-}
-
-bool pairwise_disjoint(std::vector<Span> v) {
-    std::sort(v.begin(), v.end(), [](const Span& a, const Span& b) { return a.lo < b.lo; });
-    for (size_t i = 1; i < v.size(); ++i)
-        if (v[i].lo < v[i - 1].hi) return false;
-    return true;
-}
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // K, N shared checks.  Returns DPR_OK to proceed.
 dpr_status check_kn(int K, int64_t N) {

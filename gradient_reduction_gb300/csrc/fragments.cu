@@ -24,6 +24,7 @@
 #include "dpr_device.cuh"
 #include "dpr_kernels.h"
 #include "dpr_ring.cuh"
+#include "host_checks.h"
 
 namespace dpr {
 namespace {
@@ -119,14 +120,6 @@ const void* rs_fragments_for(int K) {
     }
 }
 
-struct Span {
-    uintptr_t lo, hi;
-};
-
-bool overlap(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; }
-
-bool aligned_to(const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; }
-
 }  // namespace
 }  // namespace dpr
 
@@ -151,14 +144,6 @@ void free_fragments_plan(dpr_fragments_plan* pl) {
     if (pl->d_pieces) cudaFree(pl->d_pieces);
     if (pl->d_ptrs) cudaFree(pl->d_ptrs);
     delete pl;
-}
-
-template <typename T>
-cudaError_t upload(T** dst, const std::vector<T>& src, cudaStream_t st) {
-    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), src.size() * sizeof(T));
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice, st);
-    return e;
 }
 
 }  // namespace
@@ -190,7 +175,7 @@ dpr_status dpr_fragments_plan_create(dpr_fragments_plan** plan, int K, int P, co
         for (int r = 0; r < K; ++r) {
             const void* t = src[size_t(r) * P + p];
             if (!t) return DPR_ERR_INVALID_ARG;
-            if (!aligned_to(t, 2)) return DPR_ERR_ALIGNMENT;
+            if (!aligned(t, 2)) return DPR_ERR_ALIGNMENT;
             const uintptr_t a = reinterpret_cast<uintptr_t>(t);
             spans.push_back(Span{a, a + uintptr_t(numel[p]) * 2});
         }
@@ -233,7 +218,7 @@ dpr_status dpr_fragments_plan_create(dpr_fragments_plan** plan, int K, int P, co
             const FragPiece& first = pieces[tl.piece0];
             bool vec = tl.n_pieces == 1 && first.p >= 0 && n % 16 == 0;
             for (int r = 0; r < K && vec; ++r)
-                vec = aligned_to(static_cast<const uint16_t*>(src[size_t(r) * P + first.p]) + first.src_off, 32);
+                vec = aligned(static_cast<const uint16_t*>(src[size_t(r) * P + first.p]) + first.src_off, 32);
             tl.vec = vec ? 1 : 0;
             tl.p = vec ? first.p : -1;
             tl.src_off = vec ? first.src_off : 0;
@@ -278,17 +263,17 @@ dpr_status dpr_reduce_scatter_fragments(const dpr_fragments_plan* plan, float* c
     std::vector<Span> outs;
     for (int j = 0; j < K; ++j) {
         if (!out[j]) return DPR_ERR_INVALID_ARG;
-        if (!aligned_to(out[j], 4)) return DPR_ERR_ALIGNMENT;
-        a32 = a32 && aligned_to(out[j], 32);
+        if (!aligned(out[j], 4)) return DPR_ERR_ALIGNMENT;
+        a32 = a32 && aligned(out[j], 32);
         const uintptr_t a = reinterpret_cast<uintptr_t>(out[j]);
         outs.push_back(Span{a, a + uintptr_t(S) * 4});
     }
     for (int j = 0; j < K; ++j)
         for (int q = j + 1; q < K; ++q)
-            if (overlap(outs[j], outs[q])) return DPR_ERR_ALIAS;
+            if (overlaps(outs[j], outs[q])) return DPR_ERR_ALIAS;
     for (const Span& t : plan->src_spans)
         for (const Span& o : outs)
-            if (overlap(t, o)) return DPR_ERR_ALIAS;
+            if (overlaps(t, o)) return DPR_ERR_ALIAS;
     if (plan->tiles.empty()) return DPR_OK;
     FragParams prm;
     std::memset(&prm, 0, sizeof(prm));

@@ -1,0 +1,43 @@
+// Host-side helpers shared by the libdpr entry points: address spans and the
+// overlap and alignment tests that run before any launch, and the one-time
+// upload of a plan's tables.
+#pragma once
+
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+namespace dpr {
+
+struct Span {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+inline bool overlaps(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+inline Span span_of(const void* p, uint64_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Span{a, a + uintptr_t(bytes)};
+}
+
+inline bool pairwise_disjoint(std::vector<Span> v) {
+    std::sort(v.begin(), v.end(), [](const Span& a, const Span& b) { return a.lo < b.lo; });
+    for (size_t i = 1; i < v.size(); ++i)
+        if (v[i].lo < v[i - 1].hi) return false;
+    return true;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// cudaMalloc a device copy of `src` and enqueue the copy on `st`.
+template <typename T>
+cudaError_t upload(T** dst, const std::vector<T>& src, cudaStream_t st) {
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), src.size() * sizeof(T));
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice, st);
+    return e;
+}
+
+}  // namespace dpr
