@@ -105,6 +105,8 @@ def parse_args(argv=None):
     p.add_argument("--micro", type=int, default=1, choices=[1, 2],
                    help="point: micro-batches accumulated before the reduce")
     p.add_argument("--seed", type=int, default=0, help="point: generator seed")
+    p.add_argument("--bucket-elems", type=int, default=25_000_000,
+                   help="configs: bucket cap of configuration 3, in elements per rank")
     p.add_argument("--only", choices=STEP_KERNELS + Z3_KERNELS + BF16_KERNELS, default=None,
                    help="profile helper: launch only this kernel per step")
     p.add_argument("--graph", action="store_true",
@@ -674,7 +676,8 @@ def run_configs_bench(args):
         cfg = C.CFG3
         K = cfg.K
         numel = [n for *_, n in cfg.arrival_order()]
-        bucket_of, offset, bucket_numel = dpr.dpr_bucket_assign(numel, cfg.bucket_cap, pad_to=8 * K)
+        bucket_of, offset, bucket_numel = dpr.dpr_bucket_assign(numel, args.bucket_elems,
+                                                                pad_to=8 * K)
         grads = [[cfg.grad(r, p, device=dev) for p in range(len(numel))] for r in range(K)]
         part = torch.empty(K, sum(bucket_numel) // K, dtype=f32, device=dev)
         ipg = torch.zeros(K, max(bucket_numel), dtype=bf, device=dev)
@@ -751,7 +754,7 @@ def run_configs_bench(args):
     head = [r for r in rows if r["config"] == 3][0]
     line = {"metric": METRIC, "value": head["gbs"], "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-            "config": {"workload": "configs_1_to_4"},
+            "config": {"workload": "configs_1_to_4", "bucket_elems": args.bucket_elems},
             "value_is": "configuration 3: gather + reduce-scatter of every bucket of one backward",
             "peak": peak, "peak_kind": kind, "table": rows}
     print(json.dumps(line), flush=True)
