@@ -123,3 +123,41 @@ def test_fuzz_flatten_and_coalesced(case):
             want = ring.reduce_scatter_coalesced(grads, numel, K, mode, 1.0 / K)
             for j in range(K):
                 H.assert_f32_equal(out[j].cpu().numpy(), want[j], f"coalesced partition {j}")
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_fuzz_reduce_scatter_fragments(case):
+    """Random buckets: K, gradient count and sizes, gaps, end padding, source
+    misalignment, mode, accumulate and scale; the fragments path against the
+    oracle's gather followed by its ring reduce-scatter."""
+    dev = H.device()
+    rng = random.Random(5000 + case)
+    nrng = np.random.default_rng(50 + case)
+    K = rng.choice(KS)
+    P = rng.randint(1, 7)
+    sizes = [rng.choice([1, 7, 16, 100, 4095, 4096, 4097, 8192 + 16, 3 * 4096, 20000])
+             for _ in range(P)]
+    offset, at = [], 0
+    for n in sizes:
+        at += rng.choice([0, 0, 0, 1, 5, 16, 4096])
+        offset.append(at)
+        at += n
+    order = list(range(P))
+    rng.shuffle(order)                          # plan order need not be bucket order
+    bucket = at + rng.choice([0, 3, 64])
+    bucket += (-bucket) % K
+    S = bucket // K
+    host = [[_spread_bf16(nrng, n, spread=rng.choice([4, 12])) for n in sizes] for _ in range(K)]
+    srcs = [[_dev_bf16(host[r][p], dev, rng.choice([0, 0, 1, 8])) for p in order] for r in range(K)]
+    mode, acc = rng.choice(H.MODES), rng.random() < 0.5
+    scale = rng.choice([1.0 / K, 1.0, 0.37])
+    init = [nrng.standard_normal(S).astype(np.float32) for _ in range(K)]
+    outs = [torch.from_numpy(i.copy()).to(dev) for i in init]
+    with dpr.dpr_fragments_plan_create(srcs, [sizes[p] for p in order],
+                                       [offset[p] for p in order], bucket) as plan:
+        dpr.dpr_reduce_scatter_fragments(plan, outs, mode=mode, scale=scale, accumulate=acc)
+        torch.cuda.synchronize()
+    flat = ofl.flatten_bucket(host, sizes, offset, bucket)
+    want, _ = ring.reduce_scatter(flat, K, 1, mode, scale, out_init=init if acc else None)
+    for j in range(K):
+        H.assert_f32_equal(outs[j].cpu().numpy(), want[j], f"K={K} P={P} shard {j}")
