@@ -105,6 +105,9 @@ def parse_args(argv=None):
     p.add_argument("--micro", type=int, default=1, choices=[1, 2],
                    help="point: micro-batches accumulated before the reduce")
     p.add_argument("--seed", type=int, default=0, help="point: generator seed")
+    p.add_argument("--z3-layers", type=int, default=None,
+                   help="profile helper: layers of the zero3_per_param model (a small case); "
+                        "its bench line is quoted only at the default 7")
     p.add_argument("--bucket-elems", type=int, default=25_000_000,
                    help="configs: bucket cap of configuration 3, in elements per rank")
     p.add_argument("--only", choices=STEP_KERNELS + Z3_KERNELS + BF16_KERNELS, default=None,
@@ -402,12 +405,14 @@ class Zero3Workload:
     parameters per rank."""
     kernels = Z3_KERNELS
 
-    def __init__(self, dev, stream):
+    def __init__(self, dev, stream, layers: int | None = None):
+        import dataclasses
+
         import torch
         import gradient_reduction_gb300 as dpr
         from workloads import configs as C
         self.dpr, self.torch, self.dev, self.stream = dpr, torch, dev, stream
-        cfg = C.CFG3
+        cfg = C.CFG3 if layers is None else dataclasses.replace(C.CFG3, layers=layers)
         K = cfg.K
         arr = cfg.arrival_order()
         numel = [n for *_, n in arr]
@@ -914,7 +919,7 @@ def run_device(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
     if args.workload == "zero3_per_param":
-        wl = Zero3Workload(dev, stream)
+        wl = Zero3Workload(dev, stream, args.z3_layers)
         kernels = (args.only,) if args.only else Z3_KERNELS
     elif args.workload == "bf16_partition":
         wl = Bf16PartitionWorkload(dev, stream)
@@ -1348,8 +1353,9 @@ def main(argv=None):
             and args.workload == "zero_bucket":
         line["cpu_baseline"] = cpu_baseline(args)
     if args.workload == "zero3_per_param":
-        line["config"] = {"workload": "zero3_per_param_k8_h4096_7layer", "K": 8,
-                          "tensors_per_rank": 56, "elements_per_rank": res["wl"].N,
+        layers = args.z3_layers or 7
+        line["config"] = {"workload": f"zero3_per_param_k8_h4096_{layers}layer", "K": 8,
+                          "tensors_per_rank": 8 * layers, "elements_per_rank": res["wl"].N,
                           "step": "RS coalesced (ring_fp32, per-parameter shards) + AG coalesced",
                           "parallelism": "single GPU, 8 simulated ranks",
                           "l2": "inputs (42 GB resident) far larger than L2; no flush needed"}
