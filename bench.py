@@ -89,13 +89,15 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--workload", choices=["zero_bucket", "zero3_per_param", "bucket_pipeline",
-                                          "bf16_partition", "sweep", "configs", "point"],
+                                          "bf16_partition", "sweep", "configs", "point",
+                                          "fragments"],
                    default="zero_bucket",
                    help="zero_bucket: the headline step (default); zero3_per_param: the ZeRO-3 "
                         "discrete path on config 3's 56 gradients; bucket_pipeline: backward "
                         "time under the stream-overlap policies; bf16_partition: reduce-scatter "
                         "into bf16 partitions over two micro steps and the step-time cast; "
-                        "sweep: configuration 5; configs: configurations 1-4; point: one "
+                        "sweep: configuration 5; configs: configurations 1-4; fragments: the "
+                        "1 GiB bucket reduced straight from its fragments; point: one "
                         "reduce-scatter / all-gather / all-reduce point chosen by --K, "
                         "--bytes-per-rank, --mode, --micro, --seed")
     p.add_argument("--K", type=int, default=8, help="point: simulated ranks")
@@ -766,6 +768,52 @@ def run_configs_bench(args):
     return 0
 
 
+def run_fragments_bench(args):
+    """The bench's 1 GiB bucket (K=8, 32 fragmented 4096x4096 gradients per
+    rank) reduce-scattered two ways: gathered into the flat bucket, then
+    reduce-scattered (two launches), and straight from the fragments (one
+    launch).  Both give the same bits; the line reports both times."""
+    import torch
+    import gradient_reduction_gb300 as dpr
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = torch.cuda.Stream(device=dev)
+    wl = Workload(dev, s)
+    K, N, P, F = wl.K, wl.N, wl.P, wl.F
+    S = N // K
+    timed = LaunchTimer(s, args.steps, args.warmup)
+    with torch.cuda.stream(s):
+        out = list(torch.empty(K, S, dtype=torch.float32, device=dev).unbind(0))
+        ref = list(torch.empty(K, S, dtype=torch.float32, device=dev).unbind(0))
+        with dpr.dpr_fragments_plan_create(wl.frags, [F] * P, [p * F for p in range(P)], N,
+                                           stream=s) as plan:
+            def gather_then_rs():
+                dpr.dpr_flatten_bucket(wl.plan, wl.ipg1, stream=s)
+                dpr.dpr_reduce_scatter(wl.ipg1, K, 1, N, ref, stream=s)
+
+            def from_fragments():
+                dpr.dpr_reduce_scatter_fragments(plan, out, stream=s)
+
+            t2 = timed(gather_then_rs, 1 << 30)
+            t1 = timed(from_fragments, 1 << 30)
+            s.synchronize()
+            same = all(torch.equal(a.view(torch.int32), b.view(torch.int32)) for a, b in zip(out, ref))
+    wl.plan.close()
+    b1 = 2 * K * N + 4 * N
+    b2 = 4 * K * N + 2 * K * N + 4 * N
+    peak, kind = load_peaks()
+    line = {"metric": METRIC, "value": round(b1 / t1 / 1e9, 1), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "config": {"workload": "fragments_k8_1GiB", "K": K, "elements_per_rank": N,
+                       "fragments_per_rank": f"{P} x (4096x4096)"},
+            "value_is": "reduce-scatter straight from the fragments, GB/s of its algorithmic bytes",
+            "from_fragments": {"ms": round(t1 * 1e3, 3), "bytes": b1, "launches": 1},
+            "gather_then_reduce_scatter": {"ms": round(t2 * 1e3, 3), "bytes": b2, "launches": 2},
+            "speedup": round(t2 / t1, 3), "bit_identical": same, "peak": peak, "peak_kind": kind}
+    print(json.dumps(line), flush=True)
+    return 0 if same else 1
+
+
 def run_point_bench(args):
     """One point chosen on the command line: the reduce-scatter (--mode,
     --micro), all-gather and all-reduce at --K ranks and --bytes-per-rank,
@@ -1309,6 +1357,8 @@ def main(argv=None):
         return run_configs_bench(args)
     if args.workload == "point":
         return run_point_bench(args)
+    if args.workload == "fragments":
+        return run_fragments_bench(args)
     import torch
     rank, world, local_rank = dist_env()
     if world > 1:
