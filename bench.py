@@ -22,6 +22,13 @@ roofline = the dominant kernel's algorithmic bytes per launch / its average
          CUDA-event launch time, against the measured HBM copy peak.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl dpr|reference]
+                  [--workload zero_bucket|zero3_per_param|bucket_pipeline|bf16_partition|
+                              sweep|configs|fragments|point]
+
+The default workload is the headline step above; the others time the
+per-parameter path, the stream-overlapped bucket pipeline, the bf16
+partitions, configuration 5's sweep, configurations 1-4, the reduce-scatter
+straight from fragments, and one point chosen on the command line.
 
 --impl reference times the CPU oracle (numpy, one process per host core, each
 on its own slab) on a bounded sample of the same workload.  With --gpus N > 1 (under torchrun) every rank runs an
