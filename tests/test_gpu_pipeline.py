@@ -104,6 +104,35 @@ def test_hop_mode_accumulate_and_block_budget(max_blocks):
         p.close()
 
 
+def test_reduction_stream_orders_other_work():
+    """dpr_bucket_pipeline_stream returns the pipeline's own reduction stream:
+    work ordered behind it sees every submitted reduction complete."""
+    dev = H.device()
+    cfg, numel, buckets, grads, plans = _small_model(dev)
+    K = cfg.K
+    serial = _serial(K, buckets, plans, dev)
+    cur = torch.cuda.Stream()
+    other = torch.cuda.Stream()
+    outs = [[torch.zeros(b.numel // K, device=dev) for _ in range(K)] for b in buckets]
+    copies = []
+    with dpr.BucketPipeline(K, max(b.numel for b in buckets), 2) as pipe:
+        rs = pipe.reduction_stream()
+        assert rs.cuda_stream not in (0, cur.cuda_stream, other.cuda_stream)
+        for plan, o in zip(plans, outs):
+            pipe.submit(plan, o, stream=cur)
+        other.wait_stream(rs)            # ordered behind the reductions, not behind a flush
+        with torch.cuda.stream(other):
+            copies = [[t.clone() for t in o] for o in outs]
+        other.synchronize()
+        pipe.flush(stream=cur)
+        cur.synchronize()
+    for bi, (c, so) in enumerate(zip(copies, serial)):
+        for j in range(K):
+            assert torch.equal(c[j], so[j]), f"bucket {bi} shard {j}"
+    for p in plans:
+        p.close()
+
+
 def test_rapid_reuse_of_both_buffers():
     """The producer rewrites the same gradient tensors for every bucket on the
     compute stream; 48 buckets go through 2 physical buffers back to back."""
