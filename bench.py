@@ -1324,7 +1324,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    n = 1 << 18
+    n = 1 << 20          # per process, as in the CPU baseline of the bench line
     cores = host_cores()
     pool = OracleSlabPool(n, cores)
     try:
