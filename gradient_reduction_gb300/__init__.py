@@ -36,9 +36,12 @@ from ._binding import (  # noqa: F401
     dpr_fragments_plan_create,
     dpr_fragments_plan_destroy,
     dpr_reduce_scatter,
+    dpr_reduce_scatter_batch,
     dpr_reduce_scatter_bf16,
     dpr_reduce_scatter_coalesced,
     dpr_reduce_scatter_fragments,
+    dpr_reduce_scatter_fragments_batch,
+    dpr_set_programmatic_launch,
     dpr_strerror,
     dpr_version,
     lib,

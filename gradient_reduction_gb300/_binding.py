@@ -27,6 +27,8 @@ _i64p = ctypes.POINTER(ctypes.c_int64)
 _SIGS = {
     "dpr_reduce_scatter": [_pp, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _pp, ctypes.c_int,
                            ctypes.c_float, ctypes.c_int, _c_p],
+    "dpr_reduce_scatter_batch": [ctypes.c_int, _pp, ctypes.c_int, ctypes.c_int, _i64p, _pp,
+                                 ctypes.c_int, ctypes.c_float, ctypes.c_int, _c_p],
     "dpr_allgather": [_pp, ctypes.c_int, ctypes.c_int64, _pp, _c_p],
     "dpr_reduce_scatter_bf16": [_pp, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _pp, ctypes.c_int,
                                 ctypes.c_float, ctypes.c_int, _c_p],
@@ -44,6 +46,8 @@ _SIGS = {
     "dpr_fragments_plan_create": [ctypes.POINTER(_c_p), ctypes.c_int, ctypes.c_int, _pp, _i64p,
                                   _i64p, ctypes.c_int64, _c_p],
     "dpr_reduce_scatter_fragments": [_c_p, _pp, ctypes.c_int, ctypes.c_float, ctypes.c_int, _c_p],
+    "dpr_reduce_scatter_fragments_batch": [ctypes.c_int, _pp, _pp, ctypes.c_int, ctypes.c_float,
+                                           ctypes.c_int, _c_p],
     "dpr_fragments_plan_destroy": [_c_p],
     "dpr_coalesced_plan_create": [ctypes.POINTER(_c_p), ctypes.c_int, ctypes.c_int, _pp, _i64p,
                                   _c_p],
@@ -69,6 +73,7 @@ _SIGS = {
                            ctypes.c_double, ctypes.POINTER(ctypes.c_double)],
     "dpr_cost_dp_speedup": [ctypes.c_double, ctypes.c_int, ctypes.c_double, ctypes.c_double,
                             ctypes.c_double, ctypes.POINTER(ctypes.c_double)],
+    "dpr_set_programmatic_launch": [ctypes.c_int, ctypes.POINTER(ctypes.c_int)],
     "dpr_strerror": [ctypes.c_int],
     "dpr_last_cuda_error": [],
     "dpr_version": [],
@@ -148,6 +153,41 @@ def dpr_reduce_scatter(inputs: Sequence[torch.Tensor], K: int, M: int, N: int,
                                   1.0 / K if scale is None else scale, int(bool(accumulate)),
                                   _stream(stream))
     _check("dpr_reduce_scatter", st)
+
+
+def dpr_reduce_scatter_batch(inputs: Sequence[Sequence[torch.Tensor]], K: int, M: int,
+                             N: Sequence[int], outputs: Sequence[Sequence[torch.Tensor]],
+                             mode=RING_FP32, scale: float | None = None, accumulate: bool = False,
+                             stream=None) -> None:
+    """Member i: inputs[i][m*K + r] bf16 (N[i],), outputs[i][j] fp32 (N[i]/K,).
+    The members must be independent (no output overlapping another member's
+    outputs or any input)."""
+    n = len(N)
+    if len(inputs) != n or len(outputs) != n:
+        raise ValueError("inputs, N and outputs need one entry per member")
+    flat_in, flat_out = [], []
+    for i in range(n):
+        if N[i] > 0:
+            _need(inputs[i], M * K, torch.bfloat16, N[i], f"inputs[{i}]")
+            _need(outputs[i], K, torch.float32, N[i] // K if K else 0, f"outputs[{i}]")
+        if len(inputs[i]) != M * K or len(outputs[i]) != K:
+            raise ValueError(f"member {i}: expected {M * K} inputs and {K} outputs")
+        flat_in += list(inputs[i])
+        flat_out += list(outputs[i])
+    n_arr = (ctypes.c_int64 * max(n, 1))(*N)
+    st = lib().dpr_reduce_scatter_batch(n, _ptrs(flat_in), K, M, n_arr, _ptrs(flat_out),
+                                        _MODES[mode], 1.0 / K if scale is None else scale,
+                                        int(bool(accumulate)), _stream(stream))
+    _check("dpr_reduce_scatter_batch", st)
+
+
+def dpr_set_programmatic_launch(enable: bool) -> bool:
+    """Turns programmatic dependent launch on or off (process-wide); returns
+    the previous setting."""
+    prev = ctypes.c_int()
+    _check("dpr_set_programmatic_launch",
+           lib().dpr_set_programmatic_launch(int(bool(enable)), ctypes.byref(prev)))
+    return bool(prev.value)
 
 
 def dpr_reduce_scatter_bf16(inputs: Sequence[torch.Tensor], K: int, M: int, N: int,
@@ -307,6 +347,28 @@ def dpr_reduce_scatter_fragments(plan: FragmentsPlan, outputs: Sequence[torch.Te
     _check("dpr_reduce_scatter_fragments", st)
 
 
+def dpr_reduce_scatter_fragments_batch(plans: Sequence[FragmentsPlan],
+                                       outputs: Sequence[Sequence[torch.Tensor]], mode=RING_FP32,
+                                       scale: float | None = None, accumulate: bool = False,
+                                       stream=None) -> None:
+    """Member i: plans[i] with outputs[i][j] fp32 (bucket_numel / K,).  The
+    members must be independent (no output overlapping another member's
+    outputs or any source gradient)."""
+    n = len(plans)
+    if len(outputs) != n:
+        raise ValueError("plans and outputs need one entry per member")
+    flat_out = []
+    for i, (pl, outs) in enumerate(zip(plans, outputs)):
+        _need(outs, pl.K, torch.float32, pl.bucket_numel // pl.K, f"outputs[{i}]")
+        flat_out += list(outs)
+    K = plans[0].K if plans else 1
+    h = (ctypes.c_void_p * max(n, 1))(*[pl.handle for pl in plans])
+    st = lib().dpr_reduce_scatter_fragments_batch(n, h, _ptrs(flat_out), _MODES[mode],
+                                                  1.0 / K if scale is None else scale,
+                                                  int(bool(accumulate)), _stream(stream))
+    _check("dpr_reduce_scatter_fragments_batch", st)
+
+
 def dpr_fragments_plan_destroy(plan: FragmentsPlan) -> None:
     plan.close()
 
@@ -391,8 +453,10 @@ WAIT_REDUCTION_STREAM = 1
 
 
 class BucketPipeline:
-    """Owns a dpr_bucket_pipeline; keeps each submitted bucket's plan and
-    outputs alive until the pipeline is flushed or closed."""
+    """Owns a dpr_bucket_pipeline.  Each submitted bucket's plan and outputs
+    are kept alive in the slot of the physical buffer it used, until a later
+    submit reuses that buffer (after which the submitting stream is ordered
+    behind the old reduction) or the pipeline is flushed or closed."""
 
     def __init__(self, K: int, bucket_capacity: int, n_buffers: int = 2,
                  wait_policy: int = WAIT_PER_BUFFER, max_blocks: int = 0):
@@ -401,7 +465,8 @@ class BucketPipeline:
                lib().dpr_bucket_pipeline_create(ctypes.byref(h), K, bucket_capacity, n_buffers,
                                                 wait_policy, max_blocks))
         self.handle, self.K = h.value, K
-        self._keep = []
+        self._slots = [None] * n_buffers
+        self._next = 0
 
     def submit(self, plan: FlattenPlan, outputs: Sequence[torch.Tensor], mode=RING_FP32,
                scale: float | None = None, accumulate: bool = False, producers=(), stream=None):
@@ -413,7 +478,9 @@ class BucketPipeline:
                                               int(bool(accumulate)), parr, len(prod),
                                               _stream(stream))
         _check("dpr_bucket_pipeline_submit", st)
-        self._keep.append((plan, list(outputs)))
+        if plan.bucket_numel > 0:       # an empty bucket uses no buffer
+            self._slots[self._next] = (plan, list(outputs))
+            self._next = (self._next + 1) % len(self._slots)
 
     def reduction_stream(self) -> torch.cuda.ExternalStream:
         """The pipeline's reduction stream, for ordering or timing other work."""
@@ -423,12 +490,13 @@ class BucketPipeline:
 
     def flush(self, stream=None):
         _check("dpr_bucket_pipeline_flush", lib().dpr_bucket_pipeline_flush(self.handle, _stream(stream)))
+        self._slots = [None] * len(self._slots)
 
     def close(self):
         if self.handle:
             h, self.handle = self.handle, None
             _check("dpr_bucket_pipeline_destroy", lib().dpr_bucket_pipeline_destroy(h))
-            self._keep = []
+            self._slots = [None] * len(self._slots)
 
     def __enter__(self):
         return self

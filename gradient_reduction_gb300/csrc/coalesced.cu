@@ -61,6 +61,7 @@ struct CoalParams {
     float scale;
     int accumulate;
     int bases_aligned32;            // every out / shard base is 32-byte aligned
+    int order;                      // kAfterPrevious
 };
 
 // KC > 0: K = KC fixed at compile time (the ring's loads and adds unrolled,
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(kThreads) rs_coalesced(const __grid_constant__
     const CoalSeg sg = p.segs[tr.seg];
     if (threadIdx.x < K) base[threadIdx.x] = t + sg.j * sg.s;
     __syncthreads();
+    order_enter(p.order);           // the plan's tables above are fixed; the buffers are not
     const int64_t t0 = (tile - sg.tile0) * kCoalTile;
     const int64_t n = (sg.s - t0 < kCoalTile) ? sg.s - t0 : kCoalTile;
     float* out = p.out[sg.j] + sg.off + t0;
@@ -117,6 +119,7 @@ __global__ void __launch_bounds__(kThreads) ag_coalesced(const __grid_constant__
     const TileRef tr = p.tiles[tile];
     uint16_t* const t = p.ptrs[int64_t(r) * p.P + tr.p];
     const CoalSeg sg = p.segs[tr.seg];
+    order_enter(p.order);
     const int64_t t0 = (tile - sg.ag_tile0) * kCoalAgTile;
     const int64_t n = (sg.valid - t0 < kCoalAgTile) ? sg.valid - t0 : kCoalAgTile;
     if (n <= 0) return;
@@ -321,8 +324,8 @@ dpr_status dpr_reduce_scatter_coalesced(const dpr_coalesced_plan* plan, float* c
     const void* k = (mode == DPR_SUM_RING_FP32) ? rs_coalesced_for<DPR_SUM_RING_FP32>(K)
                                                 : rs_coalesced_for<DPR_SUM_HOP_BF16>(K);
     void* args[] = {&prm};
-    return coal_cuda(cudaLaunchKernel(k, dim3(unsigned(plan->n_tiles)), dim3(kThreads), args, 0,
-                                      static_cast<cudaStream_t>(stream)));
+    return coal_cuda(launch_kernel(k, dim3(unsigned(plan->n_tiles)), args,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 dpr_status dpr_allgather_coalesced(const dpr_coalesced_plan* plan, const void* const* shards,
@@ -356,9 +359,8 @@ dpr_status dpr_allgather_coalesced(const dpr_coalesced_plan* plan, const void* c
     prm.bases_aligned32 = a32 ? 1 : 0;
     const uint64_t blocks = uint64_t(plan->n_ag_tiles) * uint64_t(K);
     void* args[] = {&prm};
-    return coal_cuda(cudaLaunchKernel(reinterpret_cast<const void*>(ag_coalesced),
-                                      dim3(unsigned(blocks)), dim3(kThreads), args, 0,
-                                      static_cast<cudaStream_t>(stream)));
+    return coal_cuda(launch_kernel(reinterpret_cast<const void*>(ag_coalesced),
+                                   dim3(unsigned(blocks)), args, static_cast<cudaStream_t>(stream)));
 }
 
 dpr_status dpr_coalesced_plan_destroy(dpr_coalesced_plan* plan) {

@@ -1,6 +1,7 @@
 // Host side of libdpr: argument validation, layout selection and launches.
 // Every check runs before anything is enqueued; a rejected call has no effect.
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -16,6 +17,7 @@ namespace dpr {
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+std::atomic<int> g_programmatic{1};
 
 dpr_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return DPR_OK;
@@ -26,6 +28,25 @@ dpr_status cuda_status(cudaError_t e) {
 }  // namespace
 
 dpr_status record_cuda_status(cudaError_t e) { return cuda_status(e); }
+
+bool programmatic_launch_enabled() { return g_programmatic.load(std::memory_order_relaxed) != 0; }
+
+cudaError_t launch_kernel(const void* kernel, dim3 grid, void** args, cudaStream_t s,
+                          bool programmatic) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // the legacy default stream (and its aliases) keeps plain launches
+    const bool legacy = s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread;
+    cfg.attrs = attr;
+    cfg.numAttrs = (programmatic && !legacy && programmatic_launch_enabled()) ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, kernel, args);
+}
 
 namespace {
 
@@ -89,19 +110,9 @@ cudaError_t blocks_per_chunk(const void* kernel, int K, uint64_t work_per_chunk,
 using namespace dpr;
 
 
-extern "C" {
-
-dpr_status dpr_reduce_scatter(const void* const* in, int K, int M, int64_t N, float* const* out,
-                              int mode, float scale, int accumulate, void* stream) {
-    return dpr::reduce_scatter_capped(in, K, M, N, out, mode, scale, accumulate,
-                                      static_cast<cudaStream_t>(stream), 0);
-}
-
-}  // extern "C"
-
-dpr_status dpr::reduce_scatter_capped(const void* const* in, int K, int M, int64_t N,
-                                      float* const* out, int mode, float scale, int accumulate,
-                                      cudaStream_t stream, int max_blocks) {
+dpr_status dpr::prepare_reduce_scatter(const void* const* in, int K, int M, int64_t N,
+                                       float* const* out, int mode, float scale, int accumulate,
+                                       RsParams* p, int* width_out) {
     dpr_status st = check_kn(K, N);
     if (st != DPR_OK) return st;
     if (M < 1 || M > DPR_MAX_MICRO) return DPR_ERR_INVALID_ARG;
@@ -131,17 +142,79 @@ dpr_status dpr::reduce_scatter_capped(const void* const* in, int K, int M, int64
         for (const Span& o : outs)
             if (overlaps(a, o)) return DPR_ERR_ALIAS;
     }
+    std::memset(p, 0, sizeof(*p));
+    for (int i = 0; i < M * K; ++i) p->in[i] = static_cast<const uint16_t*>(in[i]);
+    for (int j = 0; j < K; ++j) p->out[j] = out[j];
+    p->S = S;
+    p->su = width > 0 ? uint32_t(S / (2 * width)) : 0;
+    p->K = K;
+    p->M = M;
+    p->scale = scale;
+    p->accumulate = accumulate ? 1 : 0;
+    p->order = kAfterPrevious;
+    *width_out = width;
+    return DPR_OK;
+}
+
+extern "C" {
+
+dpr_status dpr_reduce_scatter(const void* const* in, int K, int M, int64_t N, float* const* out,
+                              int mode, float scale, int accumulate, void* stream) {
+    return dpr::reduce_scatter_capped(in, K, M, N, out, mode, scale, accumulate,
+                                      static_cast<cudaStream_t>(stream), 0);
+}
+
+dpr_status dpr_reduce_scatter_batch(int n, const void* const* in, int K, int M, const int64_t* N,
+                                    float* const* out, int mode, float scale, int accumulate,
+                                    void* stream) {
+    if (n < 0) return DPR_ERR_INVALID_ARG;
+    if (n > DPR_MAX_BATCH) return DPR_ERR_UNSUPPORTED;
+    if (n == 0) return DPR_OK;
+    if (!in || !N || !out) return DPR_ERR_INVALID_ARG;
+    if (K < 2 || K > DPR_MAX_RANKS || M < 1 || M > DPR_MAX_MICRO) return DPR_ERR_INVALID_ARG;
+    std::vector<RsParams> prm(static_cast<size_t>(n));
+    std::vector<int> width(static_cast<size_t>(n), 0);
+    std::vector<Span> outs, ins;
+    for (int i = 0; i < n; ++i) {
+        const void* const* in_i = in + size_t(i) * M * K;
+        float* const* out_i = out + size_t(i) * K;
+        dpr_status st = prepare_reduce_scatter(in_i, K, M, N[i], out_i, mode, scale, accumulate,
+                                               &prm[i], &width[i]);
+        if (st != DPR_OK) return st;
+        if (N[i] == 0) continue;
+        for (int j = 0; j < K; ++j) outs.push_back(span_of(out_i[j], uint64_t(N[i] / K) * 4));
+        for (int q = 0; q < M * K; ++q) ins.push_back(span_of(in_i[q], uint64_t(N[i]) * 2));
+    }
+    // members are independent: no output touches another output or any input
+    if (!pairwise_disjoint(outs) || any_overlap(outs, ins)) return DPR_ERR_ALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool first = true;
+    for (int i = 0; i < n; ++i) {
+        if (N[i] == 0) continue;
+        prm[i].order = first ? kAfterPrevious : kBesidePrevious;
+        first = false;
+        const cudaError_t e = launch_reduce_scatter(prm[i], mode, width[i], s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return DPR_OK;
+}
+
+dpr_status dpr_set_programmatic_launch(int enable, int* previous) {
+    const int old = g_programmatic.exchange(enable ? 1 : 0);
+    if (previous) *previous = old;
+    return DPR_OK;
+}
+
+}  // extern "C"
+
+dpr_status dpr::reduce_scatter_capped(const void* const* in, int K, int M, int64_t N,
+                                      float* const* out, int mode, float scale, int accumulate,
+                                      cudaStream_t stream, int max_blocks, bool programmatic) {
     RsParams p;
-    std::memset(&p, 0, sizeof(p));
-    for (int i = 0; i < M * K; ++i) p.in[i] = static_cast<const uint16_t*>(in[i]);
-    for (int j = 0; j < K; ++j) p.out[j] = out[j];
-    p.S = S;
-    p.su = width > 0 ? uint32_t(S / (2 * width)) : 0;
-    p.K = K;
-    p.M = M;
-    p.scale = scale;
-    p.accumulate = accumulate ? 1 : 0;
-    return cuda_status(launch_reduce_scatter(p, mode, width, stream, max_blocks));
+    int width = 0;
+    dpr_status st = prepare_reduce_scatter(in, K, M, N, out, mode, scale, accumulate, &p, &width);
+    if (st != DPR_OK || N == 0) return st;
+    return cuda_status(launch_reduce_scatter(p, mode, width, stream, max_blocks, programmatic));
 }
 
 extern "C" {
@@ -327,6 +400,29 @@ dpr_status dpr_flatten_plan_create(dpr_flatten_plan** plan, int K, int P, const 
         }
     }
     pl->n_tiles = tiles;
+    pl->n_data_segs = int64_t(pl->segs.size());
+    // zero-fill segments: the ranges of the bucket no gradient covers, per rank
+    std::vector<std::pair<int64_t, int64_t>> gaps;
+    int64_t at = 0;
+    for (const auto& sp : spans) {
+        if (sp.first > at) gaps.push_back({at, sp.first});
+        at = std::max(at, sp.second);
+    }
+    if (at < bucket_numel) gaps.push_back({at, bucket_numel});
+    for (const auto& gap : gaps) {
+        for (int r = 0; r < K; ++r) {
+            FlatSeg g;
+            g.src = nullptr;
+            g.dst_off = gap.first;
+            g.numel = gap.second - gap.first;
+            g.tile0 = tiles;
+            g.rank = r;
+            g.pad = 0;
+            tiles += (g.numel + kFlatTile - 1) / kFlatTile;
+            pl->segs.push_back(g);
+        }
+    }
+    pl->n_tiles_zero = tiles;
     cudaError_t e = cudaGetDevice(&pl->device);
     if (e == cudaSuccess && !pl->segs.empty()) {
         const size_t bytes = pl->segs.size() * sizeof(FlatSeg);
@@ -359,7 +455,8 @@ dpr_status dpr_flatten_bucket(const dpr_flatten_plan* plan, void* const* dst, vo
         outs.push_back(span_of(dst[r], uint64_t(plan->bucket_numel) * 2));
     }
     if (!pairwise_disjoint(outs)) return DPR_ERR_ALIAS;
-    for (const FlatSeg& g : plan->segs) {
+    for (int64_t i = 0; i < plan->n_data_segs; ++i) {
+        const FlatSeg& g = plan->segs[size_t(i)];
         const Span a = span_of(g.src, uint64_t(g.numel) * 2);
         for (const Span& o : outs)
             if (overlaps(a, o)) return DPR_ERR_ALIAS;
@@ -368,7 +465,7 @@ dpr_status dpr_flatten_bucket(const dpr_flatten_plan* plan, void* const* dst, vo
     FlatParams p;
     std::memset(&p, 0, sizeof(p));
     p.segs = plan->d_segs;
-    p.n_seg = int64_t(plan->segs.size());
+    p.n_seg = plan->n_data_segs;
     p.n_tiles = plan->n_tiles;
     for (int r = 0; r < plan->K; ++r) p.dst[r] = static_cast<uint16_t*>(dst[r]);
     return cuda_status(launch_flatten(p, static_cast<cudaStream_t>(stream)));

@@ -7,6 +7,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "dpr_kernels.h"
+
 namespace dpr {
 
 // 16-byte load through the non-coherent read-only path, not kept in L1:
@@ -119,6 +121,33 @@ __device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b) {
 
 __device__ __forceinline__ uint16_t add_bf16(uint16_t a, uint16_t b) {
     return to_bf16(__fadd_rn(bf_1(a), bf_1(b)));
+}
+
+// Programmatic dependent launch (griddepcontrol, sm_90 and later).  A grid
+// launched with programmatic stream serialization may start while the grid
+// before it on the stream is still draining.
+//  - grid_wait() blocks until every prerequisite grid has completed and its
+//    memory operations are visible; it returns at once for a grid launched
+//    without the attribute.
+//  - grid_release() lets the next grid on the stream be scheduled once every
+//    block of this grid has released it (or exited).
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_release() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Called by every thread before its first access to a caller buffer, after
+// any reads of its plan's fixed tables: a kAfterPrevious grid waits for the
+// previous grid here; either kind then lets the next grid be scheduled.
+__device__ __forceinline__ void order_enter(int order) {
+    if (order == kAfterPrevious) grid_wait();
+    grid_release();
+}
+
+// Called by every thread after its last access: a kBesidePrevious grid waits
+// for the previous grid here, so that it never completes before it.
+__device__ __forceinline__ void order_exit(int order) {
+    if (order == kBesidePrevious) grid_wait();
 }
 
 __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {

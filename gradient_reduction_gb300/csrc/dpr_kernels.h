@@ -16,6 +16,19 @@ namespace dpr {
 
 constexpr int kThreads = 256;      // threads per block of every kernel
 
+// How a kernel orders itself after the grid before it on its stream when it
+// is launched as a programmatic dependent launch (see launch_kernel):
+//  kAfterPrevious   wait for the previous grid before the first access to any
+//                   caller buffer (every single call);
+//  kBesidePrevious  the previous grid is a member of the same batch call and
+//                   the host has checked that it touches none of this grid's
+//                   outputs, nor writes any of its inputs: start at once, and
+//                   wait for it only before exiting, so this grid still
+//                   completes after its predecessor and stream order of
+//                   completion stays transitive for whatever comes next.
+constexpr int kAfterPrevious = 0;
+constexpr int kBesidePrevious = 1;
+
 struct RsParams {
     const uint16_t* in[DPR_MAX_MICRO * DPR_MAX_RANKS];  // in[m*K + r]
     float* out[DPR_MAX_RANKS];                          // partition shard j
@@ -25,6 +38,7 @@ struct RsParams {
     int M;
     float scale;
     int accumulate;
+    int order;          // kAfterPrevious / kBesidePrevious
 };
 
 struct ArParams {
@@ -34,6 +48,7 @@ struct ArParams {
     uint32_t su;
     int K;
     float scale;
+    int order;
 };
 
 struct AgParams {
@@ -43,9 +58,11 @@ struct AgParams {
     uint64_t tiles_per_chunk;   // ceil(S / kAgTile) (vector kernel)
     uint64_t in_place;          // bit j: shard[j] == out[j] + j*S
     int K;
+    int order;
 };
 
-// One gradient of one rank inside a flatten plan.
+// One gradient of one rank inside a flatten plan, or (src == nullptr) one
+// range of a rank's bucket that no gradient covers, to be zeroed.
 struct FlatSeg {
     const uint16_t* src;
     int64_t dst_off;    // element offset inside the rank's flat bucket
@@ -60,6 +77,7 @@ struct FlatParams {
     int64_t n_seg;
     int64_t n_tiles;
     uint16_t* dst[DPR_MAX_RANKS];
+    int order;
 };
 
 constexpr int64_t kFlatTile = 4096;     // elements per flatten tile (8 KB), one block each
@@ -75,22 +93,40 @@ inline int access_width(int64_t S, bool aligned32, bool aligned16) {
     return 0;
 }
 
+// Launches `kernel` (kThreads threads per block) on `s` with the parameter
+// block(s) in `args`.  When programmatic launches are enabled (the default,
+// dpr_set_programmatic_launch) and `s` is not the legacy default stream, the
+// launch carries CUDA's programmatic stream serialization attribute, so the
+// grid may be scheduled while the previous grid on `s` drains; the kernel's
+// `order` field says what it waits for.  `programmatic` = false forces a
+// plain launch (work after cross-stream event waits, or after host-to-device
+// copies of data the kernel reads before its wait).
+cudaError_t launch_kernel(const void* kernel, dim3 grid, void** args, cudaStream_t s,
+                          bool programmatic = true);
+
 // Launchers: return cudaSuccess or the launch error.  `width` as above;
 // RsParams::su / ArParams::su hold S / (2 * width) when width > 0.
 // max_blocks > 0 caps the grid at about that many blocks (grid-stride).
 cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaStream_t s,
-                                  int max_blocks = 0);
+                                  int max_blocks = 0, bool programmatic = true);
 
-// dpr_reduce_scatter with a block budget (0 = the whole GPU).
+// The checks of dpr_reduce_scatter, filling `p` and the access width on
+// success; nothing is launched.
+dpr_status prepare_reduce_scatter(const void* const* in, int K, int M, int64_t N,
+                                  float* const* out, int mode, float scale, int accumulate,
+                                  RsParams* p, int* width);
+
+// dpr_reduce_scatter with a block budget (0 = the whole GPU); `programmatic`
+// as for launch_kernel.
 dpr_status reduce_scatter_capped(const void* const* in, int K, int M, int64_t N, float* const* out,
                                  int mode, float scale, int accumulate, cudaStream_t stream,
-                                 int max_blocks);
+                                 int max_blocks, bool programmatic = true);
 cudaError_t launch_allreduce(const ArParams& p, int mode, int width, cudaStream_t s);
 // bf16 partition shards (RsParams::out points at bf16 buffers).
 cudaError_t launch_reduce_scatter_bf16(const RsParams& p, int mode, int width, cudaStream_t s);
 cudaError_t launch_cast(const uint16_t* in, float* out, uint64_t n, bool vec, cudaStream_t s);
 cudaError_t launch_allgather(const AgParams& p, int width, cudaStream_t s);
-cudaError_t launch_flatten(const FlatParams& p, cudaStream_t s);
+cudaError_t launch_flatten(const FlatParams& p, cudaStream_t s, bool programmatic = true);
 
 // Maps a CUDA result to a status, remembering a failure for
 // dpr_last_cuda_error() (per calling thread).
@@ -103,13 +139,22 @@ cudaError_t blocks_per_chunk(const void* kernel, int K, uint64_t work_per_chunk,
 }  // namespace dpr
 
 // A flatten plan (see dpr_flatten_plan_create): the host and device copies of
-// its segment table.
+// its segment table.  The table lists the gradients' segments (tiles
+// [0, n_tiles)) followed by one zero-fill segment per rank and uncovered
+// range of the bucket (tiles [n_tiles, n_tiles_zero)); dpr_flatten_bucket
+// runs the first part only, the bucket pipeline both, so that a reused IPG
+// buffer holds no stale data where no gradient lands.
 struct dpr_flatten_plan {
     int K = 0;
     int P = 0;
     int device = 0;
     int64_t bucket_numel = 0;
     int64_t n_tiles = 0;
+    int64_t n_tiles_zero = 0;           // tiles including the zero-fill segments
+    int64_t n_data_segs = 0;            // segments holding gradients
     std::vector<dpr::FlatSeg> segs;     // host copy
     dpr::FlatSeg* d_segs = nullptr;     // device copy
 };
+
+// Is programmatic dependent launch enabled (process-wide)?
+bool programmatic_launch_enabled();

@@ -84,6 +84,13 @@ extern "C" dpr_status dpr_flatten_bucket_noalloc(int K, int P, const void* const
         if (!is_aligned(dst[r], 2)) return DPR_ERR_ALIGNMENT;
     }
 
+    // A captured copy would re-read the shared host table at replay, after
+    // later calls may have rewritten it: refuse capture before enqueueing.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap);
+    if (e != cudaSuccess) return record_cuda_status(e);
+    if (cap != cudaStreamCaptureStatusNone) return DPR_ERR_UNSUPPORTED;
+
     std::lock_guard<std::mutex> lock(g_mu);
     // gradient spans inside the bucket must not overlap
     int64_t ns = 0;
@@ -127,7 +134,7 @@ extern "C" dpr_status dpr_flatten_bucket_noalloc(int K, int P, const void* const
     if (n_seg == 0) return DPR_OK;
 
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    e = cudaGetDevice(&dev);
     FlatSeg* table = nullptr;
     if (e == cudaSuccess) e = table_address(dev, &table);
     // Pageable-memory copy: returns once the host table has been staged, so the
@@ -143,7 +150,10 @@ extern "C" dpr_status dpr_flatten_bucket_noalloc(int K, int P, const void* const
         prm.n_seg = n_seg;
         prm.n_tiles = tiles;
         for (int r = 0; r < K; ++r) prm.dst[r] = static_cast<uint16_t*>(dst[r]);
-        e = launch_flatten(prm, static_cast<cudaStream_t>(stream));
+        prm.order = kAfterPrevious;
+        // plain launch: the kernel reads the table before any wait, so it must
+        // not start before the copy above has landed
+        e = launch_flatten(prm, static_cast<cudaStream_t>(stream), false);
     }
-    return e == cudaSuccess ? DPR_OK : DPR_ERR_CUDA;
+    return record_cuda_status(e);
 }

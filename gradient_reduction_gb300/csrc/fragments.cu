@@ -62,6 +62,7 @@ struct FragParams {
     float scale;
     int accumulate;
     int out_aligned32;
+    int order;                  // kAfterPrevious / kBesidePrevious
 };
 
 template <int KC, int MODE>
@@ -74,13 +75,16 @@ __global__ void __launch_bounds__(kThreads) rs_fragments(const __grid_constant__
     if (tl.vec && p.out_aligned32) {
         if (threadIdx.x < K) base[threadIdx.x] = p.ptrs[int64_t(threadIdx.x) * p.P + tl.p] + tl.src_off;
         __syncthreads();
+        order_enter(p.order);           // the plan's tables above are fixed; the buffers are not
         for (int64_t u = threadIdx.x; u < tl.n / 16; u += kThreads) {
             float acc[16];
             ring_sum<KC, 1, MODE, 8, true>(base, K, j, uint64_t(16 * u), acc);
             store_shard<8>(out + 16 * u, acc, p.scale, p.accumulate);
         }
+        order_exit(p.order);
         return;
     }
+    order_enter(p.order);
     for (int q = 0; q < tl.n_pieces; ++q) {
         __syncthreads();                       // the previous piece is done with base[]
         const FragPiece pc = p.pieces[tl.piece0 + q];
@@ -105,6 +109,7 @@ __global__ void __launch_bounds__(kThreads) rs_fragments(const __grid_constant__
             *o = v;
         }
     }
+    order_exit(p.order);
 }
 
 template <int MODE>
@@ -249,8 +254,16 @@ dpr_status dpr_fragments_plan_create(dpr_fragments_plan** plan, int K, int P, co
     return DPR_OK;
 }
 
-dpr_status dpr_reduce_scatter_fragments(const dpr_fragments_plan* plan, float* const* out, int mode,
-                                        float scale, int accumulate, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The checks of dpr_reduce_scatter_fragments; on success fills the parameter
+// block and the kernel and appends the output spans to `outs` (nothing is
+// launched).  *empty is set when the plan has no tiles.
+dpr_status prepare_fragments(const dpr_fragments_plan* plan, float* const* out, int mode,
+                             float scale, int accumulate, FragParams* prm, const void** kernel,
+                             std::vector<Span>* outs, bool* empty) {
     if (!plan || !out) return DPR_ERR_INVALID_ARG;
     if (mode != DPR_SUM_RING_FP32 && mode != DPR_SUM_HOP_BF16) return DPR_ERR_INVALID_ARG;
     int dev = 0;
@@ -260,38 +273,90 @@ dpr_status dpr_reduce_scatter_fragments(const dpr_fragments_plan* plan, float* c
     const int K = plan->K;
     const int64_t S = plan->bucket_numel / K;
     bool a32 = true;
-    std::vector<Span> outs;
+    std::vector<Span> mine;
     for (int j = 0; j < K; ++j) {
         if (!out[j]) return DPR_ERR_INVALID_ARG;
         if (!aligned(out[j], 4)) return DPR_ERR_ALIGNMENT;
         a32 = a32 && aligned(out[j], 32);
-        const uintptr_t a = reinterpret_cast<uintptr_t>(out[j]);
-        outs.push_back(Span{a, a + uintptr_t(S) * 4});
+        mine.push_back(span_of(out[j], uint64_t(S) * 4));
     }
-    for (int j = 0; j < K; ++j)
-        for (int q = j + 1; q < K; ++q)
-            if (overlaps(outs[j], outs[q])) return DPR_ERR_ALIAS;
+    if (!pairwise_disjoint(mine)) return DPR_ERR_ALIAS;
     for (const Span& t : plan->src_spans)
-        for (const Span& o : outs)
+        for (const Span& o : mine)
             if (overlaps(t, o)) return DPR_ERR_ALIAS;
-    if (plan->tiles.empty()) return DPR_OK;
-    FragParams prm;
-    std::memset(&prm, 0, sizeof(prm));
-    prm.tiles = plan->d_tiles;
-    prm.pieces = plan->d_pieces;
-    prm.ptrs = plan->d_ptrs;
-    for (int j = 0; j < K; ++j) prm.out[j] = out[j];
-    prm.S = S;
-    prm.K = K;
-    prm.P = plan->P;
-    prm.scale = scale;
-    prm.accumulate = accumulate ? 1 : 0;
-    prm.out_aligned32 = a32 ? 1 : 0;
-    const void* k = (mode == DPR_SUM_RING_FP32) ? rs_fragments_for<DPR_SUM_RING_FP32>(K)
-                                                : rs_fragments_for<DPR_SUM_HOP_BF16>(K);
+    *empty = plan->tiles.empty();
+    std::memset(prm, 0, sizeof(*prm));
+    prm->tiles = plan->d_tiles;
+    prm->pieces = plan->d_pieces;
+    prm->ptrs = plan->d_ptrs;
+    for (int j = 0; j < K; ++j) prm->out[j] = out[j];
+    prm->S = S;
+    prm->K = K;
+    prm->P = plan->P;
+    prm->scale = scale;
+    prm->accumulate = accumulate ? 1 : 0;
+    prm->out_aligned32 = a32 ? 1 : 0;
+    prm->order = kAfterPrevious;
+    *kernel = (mode == DPR_SUM_RING_FP32) ? rs_fragments_for<DPR_SUM_RING_FP32>(K)
+                                          : rs_fragments_for<DPR_SUM_HOP_BF16>(K);
+    outs->insert(outs->end(), mine.begin(), mine.end());
+    return DPR_OK;
+}
+
+cudaError_t launch_fragments(const dpr_fragments_plan* plan, FragParams& prm, const void* kernel,
+                             cudaStream_t stream) {
     void* args[] = {&prm};
-    return record_cuda_status(cudaLaunchKernel(k, dim3(unsigned(plan->tiles.size())), dim3(kThreads),
-                                               args, 0, static_cast<cudaStream_t>(stream)));
+    return launch_kernel(kernel, dim3(unsigned(plan->tiles.size())), args, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+dpr_status dpr_reduce_scatter_fragments(const dpr_fragments_plan* plan, float* const* out, int mode,
+                                        float scale, int accumulate, void* stream) {
+    FragParams prm;
+    const void* k = nullptr;
+    std::vector<Span> outs;
+    bool empty = false;
+    dpr_status st = prepare_fragments(plan, out, mode, scale, accumulate, &prm, &k, &outs, &empty);
+    if (st != DPR_OK || empty) return st;
+    return record_cuda_status(launch_fragments(plan, prm, k, static_cast<cudaStream_t>(stream)));
+}
+
+dpr_status dpr_reduce_scatter_fragments_batch(int n, const dpr_fragments_plan* const* plans,
+                                              float* const* out, int mode, float scale,
+                                              int accumulate, void* stream) {
+    if (n < 0 || n > DPR_MAX_BATCH) return n < 0 ? DPR_ERR_INVALID_ARG : DPR_ERR_UNSUPPORTED;
+    if (n == 0) return DPR_OK;
+    if (!plans || !out) return DPR_ERR_INVALID_ARG;
+    std::vector<FragParams> prm(static_cast<size_t>(n));
+    std::vector<const void*> kern(static_cast<size_t>(n), nullptr);
+    std::vector<char> skip(static_cast<size_t>(n), 0);
+    std::vector<Span> outs, srcs;
+    size_t o = 0;
+    for (int i = 0; i < n; ++i) {
+        if (!plans[i]) return DPR_ERR_INVALID_ARG;
+        bool empty = false;
+        dpr_status st = prepare_fragments(plans[i], out + o, mode, scale, accumulate, &prm[i],
+                                          &kern[i], &outs, &empty);
+        if (st != DPR_OK) return st;
+        skip[i] = empty ? 1 : 0;
+        o += size_t(plans[i]->K);
+        srcs.insert(srcs.end(), plans[i]->src_spans.begin(), plans[i]->src_spans.end());
+    }
+    // members are independent: no output touches another output or any source
+    if (!pairwise_disjoint(outs) || any_overlap(outs, srcs)) return DPR_ERR_ALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool first = true;
+    for (int i = 0; i < n; ++i) {
+        if (skip[i]) continue;
+        prm[i].order = first ? kAfterPrevious : kBesidePrevious;
+        first = false;
+        const cudaError_t e = launch_fragments(plans[i], prm[i], kern[i], s);
+        if (e != cudaSuccess) return record_cuda_status(e);
+    }
+    return DPR_OK;
 }
 
 dpr_status dpr_fragments_plan_destroy(dpr_fragments_plan* plan) {

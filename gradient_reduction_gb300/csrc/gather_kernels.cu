@@ -21,6 +21,7 @@ namespace {
 // nothing to do, so no block writes memory that another block reads.
 template <int W>
 __global__ void __launch_bounds__(kThreads) ag_vec(const __grid_constant__ AgParams p) {
+    order_enter(p.order);
     const uint64_t b = blockIdx.x;
     const int r = int(b % uint64_t(p.K));
     const uint64_t g = b / uint64_t(p.K);
@@ -57,6 +58,7 @@ __global__ void __launch_bounds__(kThreads) ag_scalar(const __grid_constant__ Ag
     const int j = blockIdx.y, K = p.K;
     const uint64_t S = uint64_t(p.S), base = uint64_t(j) * S;
     const uint16_t* const src = p.shard[j];
+    order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < S;
          t += uint64_t(gridDim.x) * kThreads) {
         const uint16_t v = src[t];
@@ -70,7 +72,9 @@ __global__ void __launch_bounds__(kThreads) ag_scalar(const __grid_constant__ Ag
 // rank occupies [offset_p, offset_p + numel_p) of that rank's flat bucket.
 // The plan cuts every (rank, gradient) segment into tiles of kFlatTile
 // elements; one block copies one tile and finds its segment by binary search
-// over the segments' first-tile indices.
+// over the segments' first-tile indices.  A segment without a source is a
+// range no gradient covers, which the block zeroes (the bucket pipeline's
+// reused buffers).
 
 // Copies n <= kFlatTile elements.  When source and destination share their
 // offset modulo 32 (or 16) bytes, the bulk moves as 32-byte (16-byte) vectors
@@ -96,6 +100,21 @@ __device__ __forceinline__ void copy_vec(const uint16_t* src, uint16_t* dst, int
     if (threadIdx.x < n - done) dst[done + threadIdx.x] = src[done + threadIdx.x];
 }
 
+// Zeroes n <= kFlatTile elements: 32-byte stores between a scalar head that
+// reaches a 32-byte boundary and a scalar tail.
+__device__ __forceinline__ void zero_tile(uint16_t* dst, int64_t n) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+    int64_t h = int64_t(((32u - (a & 31u)) & 31u) >> 1);
+    if (h > n) h = n;
+    if (threadIdx.x < h) dst[threadIdx.x] = 0;
+    const int64_t nv = (n - h) / 16;
+    uint16_t* d = dst + h;
+    const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    for (int64_t v = threadIdx.x; v < nv; v += kThreads) store_words<8>(d + 16 * v, z);
+    const int64_t done = h + nv * 16;
+    if (threadIdx.x < n - done) dst[done + threadIdx.x] = 0;
+}
+
 __device__ __forceinline__ void copy_tile(const uint16_t* src, uint16_t* dst, int64_t n) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(src) ^ reinterpret_cast<uintptr_t>(dst);
     if ((x & 31u) == 0) {
@@ -119,8 +138,13 @@ __global__ void __launch_bounds__(kThreads) flatten_kernel(const __grid_constant
     const int64_t t0 = (tile - sg.tile0) * kFlatTile;
     const int64_t rem = sg.numel - t0;
     const int64_t n = rem < kFlatTile ? rem : kFlatTile;
-    const uint16_t* src = sg.src + t0;
     uint16_t* dst = p.dst[sg.rank] + sg.dst_off + t0;
+    order_enter(p.order);           // the table above is fixed; the buckets are not
+    if (sg.src == nullptr) {
+        zero_tile(dst, n);
+        return;
+    }
+    const uint16_t* src = sg.src + t0;
     const uintptr_t a = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
     if (n == kFlatTile && (a & 31u) == 0) {  // full, 32-byte aligned tile: fixed trip count
 #pragma unroll
@@ -143,20 +167,20 @@ cudaError_t launch_allgather(const AgParams& p, int width, cudaStream_t s) {
                                      : reinterpret_cast<const void*>(ag_vec<4>);
         const uint64_t blocks = uint64_t(p.K) * uint64_t(p.K) * p.tiles_per_chunk;
         void* args[] = {const_cast<AgParams*>(&p)};
-        return cudaLaunchKernel(k, dim3(unsigned(blocks)), dim3(kThreads), args, 0, s);
+        return launch_kernel(k, dim3(unsigned(blocks)), args, s);
     }
     const void* k = reinterpret_cast<const void*>(ag_scalar);
     int gx = 1;
     cudaError_t e = blocks_per_chunk(k, p.K, uint64_t(p.S), &gx);
     if (e != cudaSuccess) return e;
     void* args[] = {const_cast<AgParams*>(&p)};
-    return cudaLaunchKernel(k, dim3(gx, p.K), dim3(kThreads), args, 0, s);
+    return launch_kernel(k, dim3(gx, p.K), args, s);
 }
 
-cudaError_t launch_flatten(const FlatParams& p, cudaStream_t s) {
+cudaError_t launch_flatten(const FlatParams& p, cudaStream_t s, bool programmatic) {
     const void* k = reinterpret_cast<const void*>(flatten_kernel);
     void* args[] = {const_cast<FlatParams*>(&p)};
-    return cudaLaunchKernel(k, dim3(unsigned(p.n_tiles)), dim3(kThreads), args, 0, s);
+    return launch_kernel(k, dim3(unsigned(p.n_tiles)), args, s, programmatic);
 }
 
 }  // namespace dpr

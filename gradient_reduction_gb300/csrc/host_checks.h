@@ -29,6 +29,19 @@ inline bool pairwise_disjoint(std::vector<Span> v) {
     return true;
 }
 
+// Does any span of `b` overlap any span of `a`?  `a` must be pairwise
+// disjoint (as pairwise_disjoint checks).
+inline bool any_overlap(std::vector<Span> a, const std::vector<Span>& b) {
+    std::sort(a.begin(), a.end(), [](const Span& x, const Span& y) { return x.lo < y.lo; });
+    for (const Span& x : b) {
+        // the first span of `a` that ends after x starts (ends are sorted too)
+        auto it = std::upper_bound(a.begin(), a.end(), x.lo,
+                                   [](uintptr_t v, const Span& y) { return v < y.hi; });
+        if (it != a.end() && overlaps(*it, x)) return true;
+    }
+    return false;
+}
+
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // cudaMalloc a device copy of `src` and enqueue the copy on `st`.

@@ -24,6 +24,7 @@
 #include <vector>
 
 #include "dpr_kernels.h"
+#include "host_checks.h"
 
 using namespace dpr;
 
@@ -36,7 +37,12 @@ struct dpr_bucket_pipeline {
     int64_t capacity = 0;               // elements per rank slice of one IPG buffer
     uint16_t* ipg = nullptr;            // n_buffers * K * capacity bf16
     cudaStream_t reduction = nullptr;
+    // every event is created once, here, and re-recorded on each use (a wait
+    // enqueued earlier keeps referring to the record it saw)
     std::vector<cudaEvent_t> done;      // per physical buffer: its last reduction finished
+    std::vector<cudaEvent_t> ready;     // per physical buffer: its gather finished
+    std::vector<cudaEvent_t> produced;  // per producer slot: the producer's work so far
+    cudaEvent_t tail = nullptr;         // everything queued on the reduction stream
     std::vector<bool> used;
     int next = 0;
     uint64_t submitted = 0;
@@ -46,8 +52,10 @@ namespace {
 
 void destroy_pipeline(dpr_bucket_pipeline* pl) {
     if (!pl) return;
-    for (cudaEvent_t e : pl->done)
-        if (e) cudaEventDestroy(e);
+    for (auto* v : {&pl->done, &pl->ready, &pl->produced})
+        for (cudaEvent_t e : *v)
+            if (e) cudaEventDestroy(e);
+    if (pl->tail) cudaEventDestroy(pl->tail);
     if (pl->reduction) cudaStreamDestroy(pl->reduction);
     if (pl->ipg) cudaFree(pl->ipg);
     delete pl;
@@ -57,21 +65,14 @@ uint16_t* slice(const dpr_bucket_pipeline* pl, int b, int r) {
     return pl->ipg + (int64_t(b) * pl->K + r) * pl->capacity;
 }
 
-// Ranges of [0, bucket_numel) that no gradient of the plan covers (the padding
-// that rounds a bucket up to equal chunks, or gaps between gradients).
-std::vector<std::pair<int64_t, int64_t>> uncovered(const dpr_flatten_plan* plan) {
-    std::vector<std::pair<int64_t, int64_t>> spans;
-    for (const FlatSeg& g : plan->segs)
-        if (g.rank == 0) spans.push_back({g.dst_off, g.dst_off + g.numel});
-    std::sort(spans.begin(), spans.end());
-    std::vector<std::pair<int64_t, int64_t>> gaps;
-    int64_t at = 0;
-    for (const auto& sp : spans) {
-        if (sp.first > at) gaps.push_back({at, sp.first});
-        at = std::max(at, sp.second);
+cudaError_t make_events(std::vector<cudaEvent_t>* v, int n) {
+    for (int i = 0; i < n; ++i) {
+        cudaEvent_t ev = nullptr;
+        const cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+        v->push_back(ev);
     }
-    if (at < plan->bucket_numel) gaps.push_back({at, plan->bucket_numel});
-    return gaps;
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -100,11 +101,10 @@ dpr_status dpr_bucket_pipeline_create(dpr_bucket_pipeline** out, int K, int64_t 
         e = cudaMalloc(reinterpret_cast<void**>(&pl->ipg),
                        size_t(n_buffers) * K * size_t(pl->capacity) * 2);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&pl->reduction, cudaStreamNonBlocking);
-    for (int b = 0; b < n_buffers && e == cudaSuccess; ++b) {
-        cudaEvent_t ev = nullptr;
-        e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-        pl->done.push_back(ev);
-    }
+    if (e == cudaSuccess) e = make_events(&pl->done, n_buffers);
+    if (e == cudaSuccess) e = make_events(&pl->ready, n_buffers);
+    if (e == cudaSuccess) e = make_events(&pl->produced, DPR_PIPELINE_MAX_PRODUCERS);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->tail, cudaEventDisableTiming);
     pl->used.assign(n_buffers, false);
     if (e != cudaSuccess) {
         destroy_pipeline(pl);
@@ -118,8 +118,10 @@ dpr_status dpr_bucket_pipeline_submit(dpr_bucket_pipeline* pl, const dpr_flatten
                                       float* const* out, int mode, float scale, int accumulate,
                                       void* const* producers, int n_producers,
                                       void* current_stream) {
+    // every check first: a rejected call enqueues nothing
     if (!pl || !plan || !out || n_producers < 0 || (n_producers > 0 && !producers))
         return DPR_ERR_INVALID_ARG;
+    if (n_producers > DPR_PIPELINE_MAX_PRODUCERS) return DPR_ERR_UNSUPPORTED;
     if (plan->K != pl->K || plan->bucket_numel > pl->capacity) return DPR_ERR_INVALID_ARG;
     if (plan->bucket_numel % pl->K != 0) return DPR_ERR_INVALID_ARG;
     if (mode != DPR_SUM_RING_FP32 && mode != DPR_SUM_HOP_BF16) return DPR_ERR_INVALID_ARG;
@@ -128,19 +130,25 @@ dpr_status dpr_bucket_pipeline_submit(dpr_bucket_pipeline* pl, const dpr_flatten
     if (e != cudaSuccess) return record_cuda_status(e);
     if (dev != pl->device || dev != plan->device) return DPR_ERR_INVALID_ARG;
     if (plan->bucket_numel == 0) return DPR_OK;
+    const int K = pl->K;
+    const int64_t S = plan->bucket_numel / K;
+    std::vector<Span> outs;
+    for (int j = 0; j < K; ++j) {
+        if (!out[j]) return DPR_ERR_INVALID_ARG;
+        if (!aligned(out[j], 4)) return DPR_ERR_ALIGNMENT;
+        outs.push_back(span_of(out[j], uint64_t(S) * 4));
+    }
+    const Span ipg = span_of(pl->ipg, uint64_t(pl->n_buffers) * K * uint64_t(pl->capacity) * 2);
+    if (!pairwise_disjoint(outs) || any_overlap(outs, {ipg})) return DPR_ERR_ALIAS;
     cudaStream_t cur = static_cast<cudaStream_t>(current_stream);
     const int b = pl->next;
-    const int K = pl->K;
 
     // 1. every stream that produced this bucket's gradients finishes first
     for (int i = 0; i < n_producers && e == cudaSuccess; ++i) {
         cudaStream_t ps = static_cast<cudaStream_t>(producers[i]);
         if (ps == cur) continue;
-        cudaEvent_t ev = nullptr;
-        e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventRecord(ev, ps);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(cur, ev, 0);
-        if (ev) cudaEventDestroy(ev);   // released once the recorded work completes
+        e = cudaEventRecord(pl->produced[size_t(i)], ps);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(cur, pl->produced[size_t(i)], 0);
     }
     // 2. buffer reuse: wait for this buffer's previous reduction (per buffer),
     //    or for everything queued on the reduction stream (reverse wait)
@@ -148,36 +156,32 @@ dpr_status dpr_bucket_pipeline_submit(dpr_bucket_pipeline* pl, const dpr_flatten
         if (pl->policy == DPR_WAIT_PER_BUFFER) {
             if (pl->used[b]) e = cudaStreamWaitEvent(cur, pl->done[b], 0);
         } else if (pl->submitted > 0) {
-            cudaEvent_t ev = nullptr;
-            e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-            if (e == cudaSuccess) e = cudaEventRecord(ev, pl->reduction);
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(cur, ev, 0);
-            if (ev) cudaEventDestroy(ev);
+            e = cudaEventRecord(pl->tail, pl->reduction);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(cur, pl->tail, 0);
         }
     }
     if (e != cudaSuccess) return record_cuda_status(e);
-    // 3. gather the bucket into the physical buffer on the compute stream;
-    //    positions no gradient covers are zeroed (stale data of earlier buckets)
-    void* dst[DPR_MAX_RANKS];
-    for (int r = 0; r < K; ++r) dst[r] = slice(pl, b, r);
-    for (const auto& gap : uncovered(plan))
-        for (int r = 0; r < K && e == cudaSuccess; ++r)
-            e = cudaMemsetAsync(slice(pl, b, r) + gap.first, 0, size_t(gap.second - gap.first) * 2, cur);
-    if (e != cudaSuccess) return record_cuda_status(e);
-    dpr_status st = dpr_flatten_bucket(plan, dst, cur);
-    if (st != DPR_OK) return st;
+    // 3. one kernel on the compute stream gathers the bucket into the physical
+    //    buffer and zeroes the positions no gradient covers (stale data of
+    //    earlier buckets); plain launches, since every kernel here follows a
+    //    cross-stream wait
+    FlatParams fp;
+    std::memset(&fp, 0, sizeof(fp));
+    fp.segs = plan->d_segs;
+    fp.n_seg = int64_t(plan->segs.size());
+    fp.n_tiles = plan->n_tiles_zero;
+    for (int r = 0; r < K; ++r) fp.dst[r] = slice(pl, b, r);
+    fp.order = kAfterPrevious;
+    if (fp.n_tiles > 0) e = launch_flatten(fp, cur, false);
     // 4. the reduction stream waits for the gather, reduce-scatters, and marks
     //    the buffer's completion
-    cudaEvent_t ready = nullptr;
-    e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventRecord(ready, cur);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(pl->reduction, ready, 0);
-    if (ready) cudaEventDestroy(ready);
+    if (e == cudaSuccess) e = cudaEventRecord(pl->ready[b], cur);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(pl->reduction, pl->ready[b], 0);
     if (e != cudaSuccess) return record_cuda_status(e);
     const void* in[DPR_MAX_RANKS];
     for (int r = 0; r < K; ++r) in[r] = slice(pl, b, r);
-    st = reduce_scatter_capped(in, K, 1, plan->bucket_numel, out, mode, scale, accumulate,
-                               pl->reduction, pl->max_blocks);
+    dpr_status st = reduce_scatter_capped(in, K, 1, plan->bucket_numel, out, mode, scale,
+                                          accumulate, pl->reduction, pl->max_blocks, false);
     if (st != DPR_OK) return st;
     e = cudaEventRecord(pl->done[b], pl->reduction);
     if (e != cudaSuccess) return record_cuda_status(e);

@@ -32,6 +32,7 @@ namespace {
 template <int KC, int M, int MODE, int W>
 __global__ void __launch_bounds__(kThreads) rs_vec(const __grid_constant__ RsParams p) {
     const int j = blockIdx.y;
+    order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < p.su;
          t += uint64_t(gridDim.x) * kThreads) {
         const uint64_t e = uint64_t(j) * uint64_t(p.S) + uint64_t(2 * W) * t;
@@ -39,6 +40,7 @@ __global__ void __launch_bounds__(kThreads) rs_vec(const __grid_constant__ RsPar
         ring_sum<KC, M, MODE, W, true>(p.in, p.K, j, e, acc);
         store_shard<W>(p.out[j] + uint64_t(2 * W) * t, acc, p.scale, p.accumulate);
     }
+    order_exit(p.order);
 }
 
 // bf16 partition shards (the ZeRO-3 partition buffer): the shard is rounded
@@ -65,6 +67,7 @@ template <int KC, int M, int MODE, int W>
 __global__ void __launch_bounds__(kThreads) rs_bf16_vec(const __grid_constant__ RsParams p) {
     const int j = blockIdx.y;
     uint16_t* const out = reinterpret_cast<uint16_t*>(p.out[j]);
+    order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < p.su;
          t += uint64_t(gridDim.x) * kThreads) {
         const uint64_t e = uint64_t(j) * uint64_t(p.S) + uint64_t(2 * W) * t;
@@ -72,6 +75,7 @@ __global__ void __launch_bounds__(kThreads) rs_bf16_vec(const __grid_constant__ 
         ring_sum<KC, M, MODE, W, true>(p.in, p.K, j, e, acc);
         store_shard_bf16<W>(out + uint64_t(2 * W) * t, acc, p.scale, p.accumulate);
     }
+    order_exit(p.order);
 }
 
 template <int MODE>
@@ -79,6 +83,7 @@ __global__ void __launch_bounds__(kThreads) rs_bf16_scalar(const __grid_constant
     const int j = blockIdx.y, K = p.K, M = p.M;
     const uint64_t S = uint64_t(p.S), base = uint64_t(j) * S;
     uint16_t* const out = reinterpret_cast<uint16_t*>(p.out[j]);
+    order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < S;
          t += uint64_t(gridDim.x) * kThreads) {
         const uint64_t e = base + t;
@@ -97,6 +102,7 @@ __global__ void __launch_bounds__(kThreads) rs_bf16_scalar(const __grid_constant
         if (p.accumulate) v = add_bf16(out[t], v);
         out[t] = v;
     }
+    order_exit(p.order);
 }
 
 // step()-time cast of a bf16 partition to fp32 (exact widening); one unit of
@@ -104,6 +110,7 @@ __global__ void __launch_bounds__(kThreads) rs_bf16_scalar(const __grid_constant
 __global__ void __launch_bounds__(kThreads) cast_bf16_fp32(const uint16_t* __restrict__ in,
                                                            float* __restrict__ out, uint64_t n,
                                                            int vec) {
+    order_enter(kAfterPrevious);
     const uint64_t u = uint64_t(blockIdx.x) * kThreads + threadIdx.x;
     const uint64_t e0 = 16 * u;
     if (e0 >= n) return;
@@ -128,6 +135,7 @@ __global__ void __launch_bounds__(kThreads) rs_scalar(const __grid_constant__ Rs
     const int j = blockIdx.y, K = p.K, M = p.M;
     const uint64_t S = uint64_t(p.S), base = uint64_t(j) * S;
     float* const out = p.out[j];
+    order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < S;
          t += uint64_t(gridDim.x) * kThreads) {
         const uint64_t e = base + t;
@@ -146,6 +154,7 @@ __global__ void __launch_bounds__(kThreads) rs_scalar(const __grid_constant__ Rs
         if (p.accumulate) v = __fadd_rn(out[t], v);
         out[t] = v;
     }
+    order_exit(p.order);
 }
 
 // ---- all-reduce (fused reduce-scatter + all-gather) -----------------------------
@@ -155,6 +164,7 @@ __global__ void __launch_bounds__(kThreads) rs_scalar(const __grid_constant__ Rs
 // and the loads use the coherent path.
 template <int KC, int MODE, int W>
 __global__ void __launch_bounds__(kThreads) ar_vec(const __grid_constant__ ArParams p) {
+    order_enter(p.order);
     const uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x;
     if (t >= p.su) return;
     const int j = blockIdx.y;
@@ -174,6 +184,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads) ar_scalar(const __grid_constant__ ArParams p) {
     const int j = blockIdx.y, K = p.K;
     const uint64_t S = uint64_t(p.S), base = uint64_t(j) * S;
+    order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < S;
          t += uint64_t(gridDim.x) * kThreads) {
         const uint64_t e = base + t;
@@ -243,7 +254,7 @@ const void* ar_kernel_for(int K, int W) {
 }  // namespace
 
 cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaStream_t s,
-                                  int max_blocks) {
+                                  int max_blocks, bool programmatic) {
     const void* k;
     dim3 grid;
     if (width > 0) {
@@ -267,7 +278,7 @@ cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaSt
         if (grid.x > cap) grid.x = cap;
     }
     void* args[] = {const_cast<RsParams*>(&p)};
-    return cudaLaunchKernel(k, grid, dim3(kThreads), args, 0, s);
+    return launch_kernel(k, grid, args, s, programmatic);
 }
 
 cudaError_t launch_reduce_scatter_bf16(const RsParams& p, int mode, int width, cudaStream_t s) {
@@ -291,7 +302,7 @@ cudaError_t launch_reduce_scatter_bf16(const RsParams& p, int mode, int width, c
         grid = dim3(gx, p.K);
     }
     void* args[] = {const_cast<RsParams*>(&p)};
-    return cudaLaunchKernel(k, grid, dim3(kThreads), args, 0, s);
+    return launch_kernel(k, grid, args, s);
 }
 
 cudaError_t launch_cast(const uint16_t* in, float* out, uint64_t n, bool vec, cudaStream_t s) {
@@ -299,8 +310,7 @@ cudaError_t launch_cast(const uint16_t* in, float* out, uint64_t n, bool vec, cu
     const unsigned blocks = unsigned((units + kThreads - 1) / kThreads);
     int v = vec ? 1 : 0;
     void* args[] = {&in, &out, &n, &v};
-    return cudaLaunchKernel(reinterpret_cast<const void*>(cast_bf16_fp32), dim3(blocks),
-                            dim3(kThreads), args, 0, s);
+    return launch_kernel(reinterpret_cast<const void*>(cast_bf16_fp32), dim3(blocks), args, s);
 }
 
 cudaError_t launch_allreduce(const ArParams& p, int mode, int width, cudaStream_t s) {
@@ -319,7 +329,7 @@ cudaError_t launch_allreduce(const ArParams& p, int mode, int width, cudaStream_
         grid = dim3(gx, p.K);
     }
     void* args[] = {const_cast<ArParams*>(&p)};
-    return cudaLaunchKernel(k, grid, dim3(kThreads), args, 0, s);
+    return launch_kernel(k, grid, args, s);
 }
 
 }  // namespace dpr

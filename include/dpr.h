@@ -18,6 +18,11 @@
  *     asynchronous execution error) is observed by synchronising the stream;
  *   - the reduce-scatter, all-gather and all-reduce calls allocate nothing
  *     and launch exactly one kernel; N == 0 is a no-op that launches nothing;
+ *   - on a stream other than the legacy default stream, kernels are launched
+ *     as programmatic dependent launches (see dpr_set_programmatic_launch):
+ *     a kernel may be scheduled while the previous kernel on the stream
+ *     drains, but it touches no caller buffer before that kernel has
+ *     completed, so stream order of data is kept;
  *   - arguments are validated on the host before anything is launched; a
  *     rejected call returns its status and has no effect.  DPR_ERR_CUDA
  *     means a CUDA call failed; dpr_last_cuda_error() then returns its
@@ -54,6 +59,7 @@ typedef enum dpr_sum_mode {
 #define DPR_MAX_RANKS 64                 /* 2 <= K <= 64 */
 #define DPR_MAX_MICRO 2                  /* 1 <= M <= 2 */
 #define DPR_MAX_ELEMS (((int64_t)1) << 34) /* N per rank buffer */
+#define DPR_MAX_BATCH 4096               /* members of one batched call */
 
 /*
  * Ring reduce-scatter with averaging and the fp32 partition-gradient cast.
@@ -84,6 +90,27 @@ typedef enum dpr_sum_mode {
 dpr_status dpr_reduce_scatter(const void* const* in, int K, int M, int64_t N,
                               float* const* out, int mode, float scale, int accumulate,
                               void* stream);
+
+/*
+ * n reduce-scatters in one call: the buckets of a backward pass that are
+ * ready together (DeepSpeed ZeRO-3 source walkthrough, section 5.1: each
+ * full bucket is reduced as soon as it is flushed, one after another on the
+ * reduction stream).  The result is that of n dpr_reduce_scatter calls in
+ * order; member i uses in[i*M*K .. (i+1)*M*K), N[i] and out[i*K .. (i+1)*K)
+ * (host arrays), with K, M, mode, scale and accumulate shared, and each
+ * member is checked as dpr_reduce_scatter checks it.  In addition no output
+ * shard of any member may overlap an output shard of another member or any
+ * member's input (DPR_ERR_ALIAS), so the members are independent.  One
+ * kernel is launched per member with N[i] > 0.  Because they are
+ * independent, each member after the first is allowed to run beside the one
+ * before it (a programmatic dependent launch that does not wait): the next
+ * bucket's blocks fill the SMs while the previous bucket's last blocks
+ * drain.  Each member still completes only after the one before it, so work
+ * that follows on the stream sees all of them.  n: 0..DPR_MAX_BATCH.
+ */
+dpr_status dpr_reduce_scatter_batch(int n, const void* const* in, int K, int M, const int64_t* N,
+                                    float* const* out, int mode, float scale, int accumulate,
+                                    void* stream);
 
 /*
  * Reduce-scatter into bf16 partition shards: the literal ZeRO-3 data flow
@@ -199,11 +226,15 @@ dpr_status dpr_flatten_plan_destroy(dpr_flatten_plan* plan);
  *     streams, without ordering between them) race on the table and must be
  *     avoided;
  *   - the first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture;
+ *     (cudaGetSymbolAddress) with that device current;
  *   - the host table is copied from pageable memory, so the call returns
  *     only after the copy has been staged;
- *   - on DPR_ERR_CUDA the CUDA error is left for cudaGetLastError().
+ *   - the call cannot be captured into a CUDA graph: a captured copy would
+ *     re-read the shared host table at replay, when a later call may have
+ *     overwritten it.  On a stream that is capturing it returns
+ *     DPR_ERR_UNSUPPORTED, enqueues nothing and leaves the capture intact;
+ *   - the gather kernel is a plain launch (it reads the table the copy just
+ *     wrote), so it starts only after all earlier work on the stream.
  */
 #define DPR_NOALLOC_MAX_SEGMENTS 4096
 
@@ -243,6 +274,20 @@ dpr_status dpr_fragments_plan_create(dpr_fragments_plan** plan, int K, int P, co
 dpr_status dpr_reduce_scatter_fragments(const dpr_fragments_plan* plan, float* const* out, int mode,
                                         float scale, int accumulate, void* stream);
 dpr_status dpr_fragments_plan_destroy(dpr_fragments_plan* plan);
+
+/*
+ * n buckets reduce-scattered straight from their fragments in one call, as
+ * dpr_reduce_scatter_batch does for flat buckets: the result of n
+ * dpr_reduce_scatter_fragments calls in order, member i with plans[i] and
+ * out[i*K_i ..] (out is a host array of the members' K_i shard pointers,
+ * concatenated), mode, scale and accumulate shared.  No output shard may
+ * overlap another member's output shards or any member's source gradients
+ * (DPR_ERR_ALIAS); the members then run beside one another as described for
+ * dpr_reduce_scatter_batch.  n: 0..DPR_MAX_BATCH.
+ */
+dpr_status dpr_reduce_scatter_fragments_batch(int n, const dpr_fragments_plan* const* plans,
+                                              float* const* out, int mode, float scale,
+                                              int accumulate, void* stream);
 
 /*
  * Per-parameter partitioning (ZeRO-3): the discrete reduction path and the
@@ -308,7 +353,10 @@ dpr_status dpr_coalesced_plan_destroy(dpr_coalesced_plan* plan);
  *
  * dpr_bucket_pipeline_create allocates n_buffers (1..16) IPG buffers of K
  * rank slices of bucket_capacity bf16 elements each (cudaMalloc), a
- * non-blocking reduction stream and one completion event per buffer.
+ * non-blocking reduction stream and every event the pipeline records: a
+ * completion and a gather event per buffer, one event per producer slot
+ * (DPR_PIPELINE_MAX_PRODUCERS) and one for the reverse wait.  Submitting
+ * creates no event and allocates nothing.
  * max_blocks > 0 caps each reduction at about that many thread blocks, so the
  * reduction leaves SMs to compute running beside it (as NCCL runs its
  * collectives on a small grid); 0 lets a reduction use the whole GPU.
@@ -317,13 +365,18 @@ dpr_status dpr_coalesced_plan_destroy(dpr_coalesced_plan* plan);
  *   1. makes current_stream wait for each of the n_producers streams;
  *   2. makes current_stream wait for the chosen buffer's previous reduction
  *      (DPR_WAIT_PER_BUFFER) or for all queued reductions;
- *   3. on current_stream, zeroes bucket positions no gradient covers and
- *      gathers the bucket (dpr_flatten_bucket) into the next physical buffer;
+ *   3. on current_stream, one kernel gathers the bucket (as
+ *      dpr_flatten_bucket) into the next physical buffer and zeroes the
+ *      positions no gradient covers;
  *   4. on the reduction stream, after step 3, reduce-scatters the buffer into
  *      out (as dpr_reduce_scatter with M = 1, mode, scale, accumulate) and
  *      records the buffer's completion event.
- * Requires plan K == the pipeline's K and bucket_numel <= bucket_capacity.
- * out must stay valid until the reduction completes.
+ * Requires plan K == the pipeline's K, bucket_numel <= bucket_capacity and
+ * n_producers <= DPR_PIPELINE_MAX_PRODUCERS (else DPR_ERR_UNSUPPORTED); out
+ * (fp32 shards, 4-byte aligned) must not overlap each other or the
+ * pipeline's buffers.  Every check runs before anything is enqueued.  out
+ * must stay valid until the reduction completes.  The pipeline's kernels
+ * are plain launches (they follow cross-stream waits).
  *
  * dpr_bucket_pipeline_flush makes current_stream wait for every submitted
  * reduction (the epilogue of a backward pass).  dpr_bucket_pipeline_stream
@@ -333,6 +386,7 @@ dpr_status dpr_coalesced_plan_destroy(dpr_coalesced_plan* plan);
  */
 #define DPR_WAIT_PER_BUFFER 0
 #define DPR_WAIT_REDUCTION_STREAM 1
+#define DPR_PIPELINE_MAX_PRODUCERS 8
 
 typedef struct dpr_bucket_pipeline dpr_bucket_pipeline;
 
@@ -394,6 +448,20 @@ dpr_status dpr_cost_crossover(int algo_a, int algo_b, int K, double alpha, doubl
                               double* bytes);
 dpr_status dpr_cost_dp_speedup(double t1, int K, double bytes, double alpha, double beta,
                                double* speedup);
+
+/*
+ * Programmatic dependent launch, process-wide.  enable != 0 (the default):
+ * on every stream but the legacy default stream, each kernel is launched
+ * with CUDA's programmatic stream serialization, reads only its plan's fixed
+ * tables and its own arguments before the previous kernel on the stream has
+ * completed, and waits for that completion before touching any caller
+ * buffer; it saves the gap between a grid's drain and the next grid's start.
+ * Members after the first of a batched call do not wait (see
+ * dpr_reduce_scatter_batch).  enable == 0 launches every kernel plainly
+ * (for comparison); results are the same either way.  *previous (may be
+ * NULL) receives the setting before the call.
+ */
+dpr_status dpr_set_programmatic_launch(int enable, int* previous);
 
 /* Static description of a status code. */
 const char* dpr_strerror(int status);

@@ -35,7 +35,7 @@ def _declared():
 
 def test_exports_every_declared_function(L):
     names = _declared()
-    assert len(names) == 31
+    assert len(names) == 34
     for n in names:
         assert hasattr(L, n), n
 
@@ -257,3 +257,46 @@ def test_fragments_plan_rejections(L):
     assert h.value is None
     assert L.dpr_reduce_scatter_fragments(None, None, 0, 1.0, 0, None) == INVALID
     assert L.dpr_fragments_plan_destroy(None) == OK
+
+
+def test_reduce_scatter_batch_rejections(L):
+    """The batched reduce-scatter checks every member as the single call does,
+    and refuses members that are not independent, before any CUDA call."""
+    K, M, N = 4, 1, 64
+    rs = L.dpr_reduce_scatter_batch
+    ins = _bufs(2 * K, 1 << 20)
+    outs = _bufs(2 * K, 1 << 20, BASE + (1 << 30))
+    n2 = (ctypes.c_int64 * 2)(N, N)
+    assert rs(-1, _arr(ins), K, M, n2, _arr(outs), 0, 1.0, 0, None) == INVALID
+    assert rs(4097, _arr(ins), K, M, n2, _arr(outs), 0, 1.0, 0, None) == UNSUP
+    assert rs(0, None, K, M, None, None, 0, 1.0, 0, None) == OK
+    assert rs(2, None, K, M, n2, _arr(outs), 0, 1.0, 0, None) == INVALID
+    assert rs(2, _arr(ins), 1, M, n2, _arr(outs), 0, 1.0, 0, None) == INVALID       # K < 2
+    assert rs(2, _arr(ins), K, M, (ctypes.c_int64 * 2)(N, N + 1), _arr(outs), 0, 1.0, 0,
+              None) == INVALID                                                      # N % K
+    bad = outs[:K + 1] + [outs[K + 1] + 2] + outs[K + 2:]
+    assert rs(2, _arr(ins), K, M, n2, _arr(bad), 0, 1.0, 0, None) == ALIGN
+    # member 1 writes into member 0's output
+    clash = outs[:K] + [outs[0] + 16] + outs[K + 1:]
+    assert rs(2, _arr(ins), K, M, n2, _arr(clash), 0, 1.0, 0, None) == ALIAS
+    # member 1 writes into member 0's input
+    into_in = outs[:K] + [ins[2] + 32] + outs[K + 1:]
+    assert rs(2, _arr(ins), K, M, n2, _arr(into_in), 0, 1.0, 0, None) == ALIAS
+    # member 0 writes into member 1's input
+    into_in1 = [ins[K + 3] + 64] + outs[1:]
+    assert rs(2, _arr(ins), K, M, n2, _arr(into_in1), 0, 1.0, 0, None) == ALIAS
+
+
+def test_fragments_batch_and_launch_switch(L):
+    b = L.dpr_reduce_scatter_fragments_batch
+    assert b(0, None, None, 0, 1.0, 0, None) == OK
+    assert b(-1, None, None, 0, 1.0, 0, None) == INVALID
+    assert b(4097, None, None, 0, 1.0, 0, None) == UNSUP
+    assert b(1, None, None, 0, 1.0, 0, None) == INVALID
+    assert b(1, _arr([0]), _arr([BASE]), 0, 1.0, 0, None) == INVALID             # null plan
+    prev = ctypes.c_int()
+    assert L.dpr_set_programmatic_launch(0, ctypes.byref(prev)) == OK
+    assert prev.value == 1
+    assert L.dpr_set_programmatic_launch(1, None) == OK
+    assert L.dpr_set_programmatic_launch(1, ctypes.byref(prev)) == OK
+    assert prev.value == 1

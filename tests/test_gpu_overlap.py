@@ -1,0 +1,254 @@
+"""Programmatic dependent launch and the batched reduce-scatters, on the GPU.
+
+On a stream other than the legacy default stream every kernel of the library
+may be scheduled while the kernel before it drains; it must not touch a
+caller buffer before that kernel has completed.  These tests run chains of
+calls in which each call reads (or overwrites) what the call before it wrote,
+on a side stream with no synchronisation between the calls, with programmatic
+launch on and off, and compare every result with the oracle bit for bit.
+
+The batched reduce-scatters let independent members run beside one another.
+They are compared with the same members issued one call at a time and with
+the oracle, including members whose inputs the kernel just before the batch
+wrote, and a batch that is refused must leave every output untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gradient_reduction_gb300 as dpr
+from oracle import flatten as ofl
+from oracle import ring
+from tests import gpu_helpers as H
+from workloads import configs as C
+from workloads import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+
+def _host_bits(n, key, sigma=1e-3):
+    return syn.bf16_bits(syn.gauss_bf16(0, n, key, sigma, 0.01, 100.0))
+
+
+def _dev(a, dev):
+    return syn.bits_to_bf16(a).to(dev)
+
+
+@pytest.fixture
+def launch_mode(request):
+    prev = dpr.dpr_set_programmatic_launch(request.param)
+    yield request.param
+    dpr.dpr_set_programmatic_launch(prev)
+
+
+@pytest.mark.parametrize("launch_mode", [True, False], indirect=True,
+                         ids=["programmatic", "plain"])
+def test_dependent_chain_matches_oracle(launch_mode):
+    """flatten -> reduce-scatter (M=2, accumulate) -> in-place all-reduce of the
+    bucket -> reduce-scatter of the all-reduced bucket -> all-gather from it ->
+    flatten again (overwrites what the last two read) -> reduce-scatter, three
+    times over, back to back on one side stream."""
+    dev = H.device()
+    K = 8
+    numel = [5 * 4096 * 8, 4096 + 3, 8 * 4096 * 2 + 5, 77]
+    offset = list(np.cumsum([0] + numel[:-1]))
+    bucket = sum(numel)
+    bucket += (-bucket) % (16 * K)
+    S = bucket // K
+    host_frags = [[_host_bits(n, syn.stream_key(31, r, 0, p)) for p, n in enumerate(numel)]
+                  for r in range(K)]
+    frags = [[_dev(a, dev) for a in row] for row in host_frags]
+    host_g0 = [_host_bits(bucket, syn.stream_key(32, r, 1)) for r in range(K)]
+    ipg0 = [_dev(a, dev) for a in host_g0]
+    ipg1 = [torch.zeros(bucket, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+    init = [syn.gauss_bf16(0, S, syn.stream_key(33, j), 1e-2).float().numpy() for j in range(K)]
+    part = [torch.from_numpy(a.copy()).to(dev) for a in init]
+    part2 = [torch.empty(S, dtype=torch.float32, device=dev) for _ in range(K)]
+    part3 = [torch.empty(S, dtype=torch.float32, device=dev) for _ in range(K)]
+    full = [torch.empty(bucket, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    iters = 3
+    with dpr.dpr_flatten_plan_create(frags, numel, offset, bucket) as plan:
+        with torch.cuda.stream(s):
+            for _ in range(iters):
+                dpr.dpr_flatten_bucket(plan, ipg1, stream=s)
+                dpr.dpr_reduce_scatter(ipg0 + ipg1, K, 2, bucket, part, mode=ring.RING_FP32,
+                                       accumulate=True, stream=s)
+                dpr.dpr_allreduce(ipg1, K, bucket, ipg1, mode=ring.RING_FP32, stream=s)
+                dpr.dpr_reduce_scatter(ipg1, K, 1, bucket, part2, mode=ring.HOP_BF16, stream=s)
+                dpr.dpr_allgather([ipg1[j][j * S:(j + 1) * S] for j in range(K)], K, bucket,
+                                  full, stream=s)
+                dpr.dpr_flatten_bucket(plan, ipg1, stream=s)
+                dpr.dpr_reduce_scatter(ipg1, K, 1, bucket, part3, mode=ring.RING_FP32, stream=s)
+        s.synchronize()
+    flat = ofl.flatten_bucket(host_frags, numel, offset, bucket)
+    acc = init
+    for _ in range(iters):
+        acc, _ = ring.reduce_scatter(host_g0 + flat, K, 2, ring.RING_FP32, 1.0 / K, out_init=acc)
+    ar, _ = ring.allreduce(flat, K, ring.RING_FP32, 1.0 / K)
+    want2, _ = ring.reduce_scatter(ar, K, 1, ring.HOP_BF16, 1.0 / K)
+    want_full, _ = ring.allgather([ar[j][j * S:(j + 1) * S] for j in range(K)], K)
+    want3, _ = ring.reduce_scatter(flat, K, 1, ring.RING_FP32, 1.0 / K)
+    for j in range(K):
+        H.assert_f32_equal(part[j].cpu().numpy(), acc[j], f"accumulated shard {j}")
+        H.assert_f32_equal(part2[j].cpu().numpy(), want2[j], f"shard {j} of the all-reduced bucket")
+        H.assert_f32_equal(part3[j].cpu().numpy(), want3[j], f"shard {j} after the re-gather")
+        H.assert_bf16_equal(H.bits(full[j]), want_full[j], f"all-gather replica {j}")
+        H.assert_bf16_equal(H.bits(ipg1[j]), flat[j], f"re-gathered bucket {j}")
+
+
+def _batch_case(K, M, sizes, seed, dev):
+    """Member inputs laid out in one buffer per rank, written there by one
+    flatten launch (the kernel right before the batch).  Member i, micro m,
+    starts at an element offset that is a multiple of 16, or of 16 plus one
+    for members whose size is odd (the element-wise kernels)."""
+    n = len(sizes)
+    off, at = {}, 0
+    for i, N in enumerate(sizes):
+        for m in range(M):
+            at += (-at) % 16
+            if N % 2:
+                at += 1
+            off[i, m] = at
+            at += N
+    total = at + 16
+    host = {(r, i, m): _host_bits(sizes[i], syn.stream_key(seed, r, m, i))
+            for r in range(K) for i in range(n) for m in range(M)}
+    srcs = [[_dev(host[r, i, m], dev) for i in range(n) for m in range(M)] for r in range(K)]
+    numel = [sizes[i] for i in range(n) for m in range(M)]
+    offsets = [off[i, m] for i in range(n) for m in range(M)]
+    big = [torch.zeros(total, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+    inputs = [[big[r][off[i, m]:off[i, m] + sizes[i]] for m in range(M) for r in range(K)]
+              for i in range(n)]
+    host_in = [[host[r, i, m] for m in range(M) for r in range(K)] for i in range(n)]
+    return srcs, numel, offsets, total, big, inputs, host_in
+
+
+BATCHES = [  # (K, M, mode, accumulate, member sizes)
+    (8, 2, ring.RING_FP32, False, [8 * 16 * 700, 0, 8 * 8 * 33, 8 * 13, 8 * 4096 * 9 + 8 * 16, 8 * 16]),
+    (8, 1, ring.HOP_BF16, True, [8 * 16 * 4096] * 6 + [8 * 3]),
+    (4, 1, ring.RING_FP32, True, [4 * 16 * 999, 4 * 7, 4 * 8 * 4097]),
+    (5, 2, ring.HOP_BF16, False, [5 * 16 * 301, 5 * 9, 5 * 16 * 4096]),
+    (64, 1, ring.RING_FP32, False, [64 * 16 * 40, 64 * 16 * 3]),
+]
+
+
+@pytest.mark.parametrize("K,M,mode,accumulate,sizes", BATCHES)
+def test_reduce_scatter_batch_matches_single_calls_and_oracle(K, M, mode, accumulate, sizes):
+    dev = H.device()
+    srcs, numel, offsets, total, big, inputs, host_in = _batch_case(K, M, sizes, 60 + K, dev)
+    init = [[syn.gauss_bf16(0, N // K, syn.stream_key(61, i, 0, j), 1e-2).float().numpy()
+             for j in range(K)] for i, N in enumerate(sizes)]
+    outs = [[torch.from_numpy(a.copy()).to(dev) for a in row] for row in init]
+    ref = [[torch.from_numpy(a.copy()).to(dev) for a in row] for row in init]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    iters = 2
+    with dpr.dpr_flatten_plan_create(srcs, numel, offsets, total) as plan:
+        for _ in range(iters):
+            dpr.dpr_flatten_bucket(plan, big, stream=s)
+            dpr.dpr_reduce_scatter_batch(inputs, K, M, sizes, outs, mode=mode,
+                                         accumulate=accumulate, stream=s)
+        s.synchronize()
+        for _ in range(iters):
+            for i, N in enumerate(sizes):
+                dpr.dpr_reduce_scatter(inputs[i], K, M, N, ref[i], mode=mode,
+                                       accumulate=accumulate, stream=s)
+        s.synchronize()
+    for i, N in enumerate(sizes):
+        want = init[i]
+        for _ in range(iters if accumulate else 1):
+            want, _ = ring.reduce_scatter(host_in[i], K, M, mode, 1.0 / K,
+                                          out_init=want if accumulate else None)
+        for j in range(K):
+            assert torch.equal(outs[i][j].view(torch.int32), ref[i][j].view(torch.int32)), \
+                f"member {i} shard {j}: batch differs from single calls"
+            H.assert_f32_equal(outs[i][j].cpu().numpy(), want[j], f"member {i} shard {j}")
+
+
+def test_refused_batch_leaves_every_output_untouched():
+    dev = H.device()
+    K, N = 4, 4 * 16 * 64
+    x = [torch.ones(N, dtype=torch.bfloat16, device=dev) for _ in range(2 * K)]
+    outs = [[torch.full((N // K,), 3.0, device=dev) for _ in range(K)] for _ in range(2)]
+    # member 1 writes member 0's shard 1
+    clash = [outs[0], [outs[1][0], outs[0][1], outs[1][2], outs[1][3]]]
+    # member 1 writes into member 0's input (x[0] holds N bf16 = N/2 fp32 slots)
+    into_input = [outs[0], [outs[1][0], outs[1][1], outs[1][2],
+                            x[0].view(torch.float32)[: N // K]]]
+    for bad in (clash, into_input):
+        with pytest.raises(dpr.DprError) as e:
+            dpr.dpr_reduce_scatter_batch([x[:K], x[K:]], K, 1, [N, N], bad)
+        assert e.value.status == 5
+    torch.cuda.synchronize()
+    for row in outs:
+        for t in row:
+            assert bool((t == 3.0).all())
+    assert all(bool((t == 1.0).all()) for t in x)
+
+
+def _fragment_buckets(dev, K):
+    cfg = C.Fragmented("batch", 13, K=K, layers=3, dist=C.Dist("gauss", 1e-3), bucket_cap=20_000,
+                       hidden=96, ffn=256)
+    arr = cfg.arrival_order()
+    numel = [n for *_, n in arr]
+    buckets = ofl.assign_buckets(numel, cfg.bucket_cap, pad_to=K)
+    grads = [[cfg.grad(r, p, device=dev) for p in range(len(arr))] for r in range(K)]
+    return numel, buckets, grads
+
+
+@pytest.mark.parametrize("mode,accumulate", [(ring.RING_FP32, False), (ring.HOP_BF16, True)])
+@pytest.mark.parametrize("launch_mode", [True, False], indirect=True,
+                         ids=["programmatic", "plain"])
+def test_fragments_batch_matches_single_calls_and_oracle(mode, accumulate, launch_mode):
+    dev = H.device()
+    K = 4
+    numel, buckets, grads = _fragment_buckets(dev, K)
+    assert len(buckets) >= 3
+    plans = [dpr.dpr_fragments_plan_create([[grads[r][p] for p in b.params] for r in range(K)],
+                                           [numel[p] for p in b.params], b.offsets, b.numel)
+             for b in buckets]
+    init = [[syn.gauss_bf16(0, b.numel // K, syn.stream_key(62, bi, 0, j), 1e-2).float().numpy()
+             for j in range(K)] for bi, b in enumerate(buckets)]
+    outs = [[torch.from_numpy(a.copy()).to(dev) for a in row] for row in init]
+    ref = [[torch.from_numpy(a.copy()).to(dev) for a in row] for row in init]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    dpr.dpr_reduce_scatter_fragments_batch(plans, outs, mode=mode, accumulate=accumulate, stream=s)
+    for pl, o in zip(plans, ref):
+        dpr.dpr_reduce_scatter_fragments(pl, o, mode=mode, accumulate=accumulate, stream=s)
+    s.synchronize()
+    for bi, b in enumerate(buckets):
+        flat = ofl.flatten_bucket([[H.bits(grads[r][p]) for p in b.params] for r in range(K)],
+                                  [numel[p] for p in b.params], b.offsets, b.numel)
+        want, _ = ring.reduce_scatter(flat, K, 1, mode, 1.0 / K,
+                                      out_init=init[bi] if accumulate else None)
+        for j in range(K):
+            assert torch.equal(outs[bi][j].view(torch.int32), ref[bi][j].view(torch.int32)), \
+                f"bucket {bi} shard {j}: batch differs from single calls"
+            H.assert_f32_equal(outs[bi][j].cpu().numpy(), want[j], f"bucket {bi} shard {j}")
+    for pl in plans:
+        pl.close()
+
+
+def test_fragments_batch_refuses_an_output_inside_a_source():
+    """Member 1's first shard placed over a gradient that member 0 reads."""
+    dev = H.device()
+    K = 4
+    numel, buckets, grads = _fragment_buckets(dev, K)
+    plans = [dpr.dpr_fragments_plan_create([[grads[r][p] for p in b.params] for r in range(K)],
+                                           [numel[p] for p in b.params], b.offsets, b.numel)
+             for b in buckets[:2]]
+    outs = [[torch.full((b.numel // K,), 3.0, device=dev) for _ in range(K)] for b in buckets[:2]]
+    n1 = buckets[1].numel // K
+    g = max((grads[0][p] for p in buckets[0].params), key=lambda t: t.numel())
+    assert g.numel() % 2 == 0 and g.numel() // 2 >= n1
+    bad = [outs[0], [g.view(torch.float32)[:n1]] + outs[1][1:]]
+    with pytest.raises(dpr.DprError) as e:
+        dpr.dpr_reduce_scatter_fragments_batch(plans, bad)
+    assert e.value.status == 5
+    torch.cuda.synchronize()
+    assert all(bool((t == 3.0).all()) for row in outs for t in row)
+    for pl in plans:
+        pl.close()

@@ -232,3 +232,39 @@ def test_compute_is_not_held_behind_the_previous_reduction():
     pb.close()
     print(t)
     assert t["per_buffer"] <= 0.95 * t["reverse_wait"]
+
+
+def test_refused_submits_enqueue_nothing():
+    """Every check of a submit runs before anything is enqueued: outputs that
+    overlap each other and more producer streams than the pipeline holds
+    events for are refused, nothing is written, and the buckets submitted
+    around them still match overlap off."""
+    dev = H.device()
+    cfg, numel, buckets, grads, plans = _small_model(dev)
+    K = cfg.K
+    serial = _serial(K, buckets, plans, dev)
+    cur = torch.cuda.Stream()
+    outs = [[torch.full((b.numel // K,), 7.0, device=dev) for _ in range(K)] for b in buckets]
+    spare = torch.full((buckets[0].numel // K + 1,), 5.0, device=dev)
+    producers = [torch.cuda.Stream() for _ in range(9)]
+    with dpr.BucketPipeline(K, max(b.numel for b in buckets), 2) as pipe:
+        for bi, (plan, o) in enumerate(zip(plans, outs)):
+            if bi == 1:
+                with pytest.raises(dpr.DprError) as e:
+                    pipe.submit(plan, [o[0], o[0]] + o[2:], stream=cur)
+                assert e.value.status == 5
+                with pytest.raises(dpr.DprError) as e:       # shards 0 and 1 overlap
+                    pipe.submit(plan, [spare[:-1], spare[1:]] + o[2:], stream=cur)
+                assert e.value.status == 5
+                with pytest.raises(dpr.DprError) as e:
+                    pipe.submit(plan, o, producers=producers, stream=cur)
+                assert e.value.status == 3
+            pipe.submit(plan, o, stream=cur)
+        pipe.flush(stream=cur)
+        cur.synchronize()
+    assert bool((spare == 5.0).all())
+    for bi, (o, so) in enumerate(zip(outs, serial)):
+        for j in range(K):
+            assert torch.equal(o[j], so[j]), f"bucket {bi} shard {j}"
+    for p in plans:
+        p.close()

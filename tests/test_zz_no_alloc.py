@@ -5,17 +5,21 @@ start-up, or a loop that cannot pay for cudaMalloc/cudaFree synchronising the
 device.  It keeps its segment table in a fixed array inside the library.
 
 These tests call it through the C ABI and compare its output, bit for bit,
-with the plan-based gather (dpr_flatten_plan_create + dpr_flatten_bucket) on
-two calls in a row, and check that a call beyond the fixed table is refused.
-The file's name sorts it last, so a failure here cannot stop a run that halts
-at the first failure before the other GPU tests have run; it also passes on
-its own in a fresh process."""
+with the plan-based gather (dpr_flatten_plan_create + dpr_flatten_bucket) and
+with the oracle's gather on two calls in a row; check that a call beyond the
+fixed table is refused, that a failing call leaves its CUDA error for
+dpr_last_cuda_error(), and that a call on a capturing stream is refused
+without breaking the capture.  The file's name sorts it last, so a failure
+here cannot stop a run that halts at the first failure before the other GPU
+tests have run; it also passes on its own in a fresh process."""
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 import gradient_reduction_gb300 as dpr
+from oracle import flatten as ofl
 from tests import gpu_helpers as H
 from workloads import synthetic as syn
 
@@ -43,13 +47,17 @@ def _case(K, numel, seed, dev):
 
 
 def _call_noalloc(L, srcs, numel, offsets, bucket, dst, stream):
+    return _call_noalloc_raw(L, srcs, numel, offsets, bucket, dst, stream.cuda_stream)
+
+
+def _call_noalloc_raw(L, srcs, numel, offsets, bucket, dst, stream_handle):
     K, P = len(srcs), len(numel)
     src_ptrs = (ctypes.c_void_p * (K * P))(*[t.data_ptr() for row in srcs for t in row])
     dst_ptrs = (ctypes.c_void_p * K)(*[t.data_ptr() for t in dst])
     n_arr = (ctypes.c_int64 * P)(*numel)
     o_arr = (ctypes.c_int64 * P)(*offsets)
     return L.dpr_flatten_bucket_noalloc(K, P, src_ptrs, n_arr, o_arr, bucket, dst_ptrs,
-                                        stream.cuda_stream)
+                                        stream_handle)
 
 
 def test_noalloc_matches_plan_based_gather_two_calls_in_a_row():
@@ -71,8 +79,11 @@ def test_noalloc_matches_plan_based_gather_two_calls_in_a_row():
         with dpr.dpr_flatten_plan_create(srcs, numel, offsets, bucket) as plan:
             dpr.dpr_flatten_bucket(plan, ref)
             torch.cuda.synchronize()
+        want = ofl.flatten_bucket([[H.bits(t) for t in row] for row in srcs], numel, offsets,
+                                  bucket)
         for r in range(K):
             assert torch.equal(got[r].view(torch.int16), ref[r].view(torch.int16)), f"rank {r}"
+            assert np.array_equal(H.bits(got[r]), want[r]), f"rank {r} differs from the oracle"
 
 
 def test_noalloc_takes_no_device_memory_after_setup():
@@ -99,3 +110,51 @@ def test_noalloc_refuses_tables_beyond_the_fixed_array():
     assert _call_noalloc(L, srcs, [1] * P, list(range(P)), P, dst, torch.cuda.Stream()) == UNSUPPORTED
     with pytest.raises(dpr.DprError):
         dpr.dpr_flatten_bucket_noalloc(srcs, [1] * P, list(range(P)), P, dst)
+
+
+def test_noalloc_is_refused_on_a_capturing_stream_and_the_capture_survives():
+    """A captured call would replay a copy of the shared host table that later
+    calls overwrite, so the call refuses a capturing stream; the capture goes
+    on and the graph it makes replays."""
+    dev = H.device()
+    srcs, offsets, bucket = _case(2, [5000, 300], 9, dev)
+    dst = [torch.zeros(bucket, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    x = torch.ones(1024, device=dev)
+    g = torch.cuda.CUDAGraph()
+    refused = None
+    with torch.cuda.graph(g):
+        try:
+            dpr.dpr_flatten_bucket_noalloc(srcs, [5000, 300], offsets, bucket, dst)
+        except dpr.DprError as e:
+            refused = e.status
+        x.mul_(2.0)
+    assert refused == UNSUPPORTED
+    g.replay()
+    torch.cuda.synchronize()
+    assert float(x[0]) == 2.0
+    assert all(int(t.view(torch.int16).abs().sum()) == 0 for t in dst)   # nothing was written
+
+
+def test_noalloc_records_its_cuda_error():
+    """A failing CUDA call inside the entry point is reported as DPR_ERR_CUDA
+    with its code kept for dpr_last_cuda_error(), like every other call.  The
+    failure is made on the host: while another stream captures in global
+    mode, asking whether the legacy default stream is capturing fails with
+    cudaErrorStreamCaptureImplicit, before anything is enqueued."""
+    dev = H.device()
+    L = dpr.lib()
+    srcs, offsets, bucket = _case(2, [64, 32], 3, dev)
+    dst = [torch.zeros(bucket, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    x = torch.ones(16, device=dev)
+    g = torch.cuda.CUDAGraph()
+    st = code = None
+    try:
+        with torch.cuda.graph(g, capture_error_mode="global"):
+            st = _call_noalloc_raw(L, srcs, [64, 32], offsets, bucket, dst, 0)
+            code = L.dpr_last_cuda_error()
+            x.add_(1.0)
+    except RuntimeError:
+        pass            # the capture's fate is not what this test checks
+    torch.cuda.synchronize()
+    assert st == 4, st
+    assert code == 906, code          # cudaErrorStreamCaptureImplicit
