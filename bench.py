@@ -756,6 +756,19 @@ def run_configs_bench(args):
         t_b = timed(backward_batched, fbytes)
         row(3, "rs_fp32 from fragments, all buckets in one batched call", fbytes, t_b,
             launches=len(fused))
+        s.synchronize()
+        graph_b = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_b, stream=s):
+            backward_batched()
+
+        def replay_b():
+            with torch.cuda.stream(s):
+                graph_b.replay()
+
+        t_bg = timed(replay_b, fbytes)
+        row(3, "rs_fp32 from fragments, one batched call, CUDA graph", fbytes, t_bg,
+            launches=len(fused))
+        del graph_b
         # the 42 launches captured once in a CUDA graph and replayed
         s.synchronize()
         graph = torch.cuda.CUDAGraph()
@@ -897,18 +910,47 @@ def run_sequence_bench(args):
         s.synchronize()
         return a.elapsed_time(e) / 1e3 / args.steps
 
+    def graphed(fn):
+        """fn's launches captured once in a CUDA graph (programmatic launches
+        become programmatic edges), so the host's per-call cost drops out."""
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+
+        def replay():
+            with torch.cuda.stream(s):
+                g.replay()
+        return replay, g
+
     rs_bytes = nb * (2 * M * K * N + 4 * N)
     ag_bytes = nb * (2 * N + 2 * K * N)
+    graphs = []
     prev = dpr.dpr_set_programmatic_launch(False)
     try:
         t_rs_plain = timed(lambda: rs_single("plain"))
         t_ag_plain = timed(ag_single)
+        r, g = graphed(lambda: rs_single("plain"))
+        graphs.append(g)
+        t_rs_plain_g = timed(r)
+        r, g = graphed(ag_single)
+        graphs.append(g)
+        t_ag_plain_g = timed(r)
     finally:
         dpr.dpr_set_programmatic_launch(prev)
     dpr.dpr_set_programmatic_launch(True)
     t_rs_pdl = timed(lambda: rs_single("pdl"))
     t_rs_batch = timed(rs_batch)
     t_ag_pdl = timed(ag_single)
+    r, g = graphed(lambda: rs_single("pdl"))
+    graphs.append(g)
+    t_rs_pdl_g = timed(r)
+    r, g = graphed(rs_batch)
+    graphs.append(g)
+    t_rs_batch_g = timed(r)
+    r, g = graphed(ag_single)
+    graphs.append(g)
+    t_ag_pdl_g = timed(r)
     dpr.dpr_set_programmatic_launch(prev)
     same = all(torch.equal(outs["plain"].view(torch.int32), outs[k].view(torch.int32))
                for k in ("pdl", "batch"))
@@ -929,9 +971,19 @@ def run_sequence_bench(args):
             "reduce_scatter": {"plain_launches": fig(rs_bytes, t_rs_plain),
                                "programmatic_launches": fig(rs_bytes, t_rs_pdl),
                                "one_batched_call": fig(rs_bytes, t_rs_batch),
+                               "graph_plain_launches": fig(rs_bytes, t_rs_plain_g),
+                               "graph_programmatic_launches": fig(rs_bytes, t_rs_pdl_g),
+                               "graph_one_batched_call": fig(rs_bytes, t_rs_batch_g),
                                "bytes": rs_bytes, "bit_identical": same},
             "allgather": {"plain_launches": fig(ag_bytes, t_ag_plain),
-                          "programmatic_launches": fig(ag_bytes, t_ag_pdl), "bytes": ag_bytes}}
+                          "programmatic_launches": fig(ag_bytes, t_ag_pdl),
+                          "graph_plain_launches": fig(ag_bytes, t_ag_plain_g),
+                          "graph_programmatic_launches": fig(ag_bytes, t_ag_pdl_g),
+                          "bytes": ag_bytes},
+            "host_note": "eager rows include the Python binding's per-call cost (one call per "
+                         "bucket, except the batched call); graph rows replay the same launches "
+                         "from a CUDA graph"}
+    del graphs
     print(json.dumps(line), flush=True)
     return 0 if same else 1
 

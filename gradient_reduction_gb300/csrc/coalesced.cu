@@ -29,7 +29,10 @@
 namespace dpr {
 namespace {
 
-constexpr int64_t kCoalTile = 4096;     // reduce-scatter tile: K * 8 KB read per block
+#ifndef DPR_COAL_TILE
+#define DPR_COAL_TILE 4096
+#endif
+constexpr int64_t kCoalTile = DPR_COAL_TILE;   // reduce-scatter tile: K * 2 * kCoalTile bytes read per block
 constexpr int64_t kCoalAgTile = 8192;   // all-gather tile: 16 KB written per block
 
 struct CoalSeg {

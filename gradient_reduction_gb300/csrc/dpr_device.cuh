@@ -136,18 +136,33 @@ __device__ __forceinline__ void grid_release() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Called by every thread before its first access to a caller buffer, after
-// any reads of its plan's fixed tables: a kAfterPrevious grid waits for the
-// previous grid here; either kind then lets the next grid be scheduled.
-__device__ __forceinline__ void order_enter(int order) {
-    if (order == kAfterPrevious) grid_wait();
-    grid_release();
+// Called by every thread on entry: a kBesidePrevious grid lets the next grid
+// be scheduled at once (it waits for nothing, so nothing behind it can run
+// ahead of what it itself depends on).
+__device__ __forceinline__ void order_start(int order) {
+    if (order == kBesidePrevious) grid_release();
 }
 
-// Called by every thread after its last access: a kBesidePrevious grid waits
-// for the previous grid here, so that it never completes before it.
+// Called by every thread before its first access to a caller buffer, after
+// any reads of its plan's fixed tables: a kAfterPrevious grid waits for the
+// previous grid here and only then lets the next grid be scheduled (a batch
+// member behind it relies on that wait for the buffers written before the
+// batch).
+__device__ __forceinline__ void order_enter(int order) {
+    if (order == kAfterPrevious) {
+        grid_wait();
+        grid_release();
+    }
+}
+
+// Called by every thread after its last access.  In a kBesidePrevious grid
+// the first block waits here for the previous grid, so this grid cannot
+// complete before it; the other blocks exit at once and free their SM slots
+// for the grids behind them (one waiting block is enough, since a grid
+// completes only when its last block exits).
 __device__ __forceinline__ void order_exit(int order) {
-    if (order == kBesidePrevious) grid_wait();
+    if (order == kBesidePrevious && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        grid_wait();
 }
 
 __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {

@@ -22,8 +22,8 @@ constexpr int kThreads = 256;      // threads per block of every kernel
 //                   caller buffer (every single call);
 //  kBesidePrevious  the previous grid is a member of the same batch call and
 //                   the host has checked that it touches none of this grid's
-//                   outputs, nor writes any of its inputs: start at once, and
-//                   wait for it only before exiting, so this grid still
+//                   outputs, nor writes any of its inputs: start at once; one
+//                   block waits for it before exiting, so this grid still
 //                   completes after its predecessor and stream order of
 //                   completion stays transitive for whatever comes next.
 constexpr int kAfterPrevious = 0;

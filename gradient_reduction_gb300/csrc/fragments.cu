@@ -29,19 +29,32 @@
 namespace dpr {
 namespace {
 
-constexpr int64_t kFragTile = 4096;
+#ifndef DPR_FRAG_TILE
+#define DPR_FRAG_TILE 4096
+#endif
+constexpr int64_t kFragTile = DPR_FRAG_TILE;     // elements per chunk tile, one block each
+// Blocks per SM the fragments kernels are compiled for, for K <= 8: 5 caps
+// them at 48 registers, one block more per SM than their natural 54-56,
+// which hides the per-block table reads that come before the first data
+// load.  Larger K keeps the compiler's choice (a cap would spill).
+#ifndef DPR_FRAG_MIN_BLOCKS
+#define DPR_FRAG_MIN_BLOCKS 5
+#endif
+constexpr int frag_min_blocks(int KC) { return (KC > 0 && KC <= 8) ? DPR_FRAG_MIN_BLOCKS : 1; }
 
+// 24 bytes, so that the record each block reads before its first data load
+// shares a DRAM sector with its neighbours'.
 struct FragTile {
-    int64_t t0;         // first element of the tile inside its chunk
-    int64_t n;          // elements in the tile
     int64_t src_off;    // vec tiles: offset of the tile inside gradient p
-    int32_t piece0;     // first piece
+    int32_t t0_tiles;   // first element of the tile inside its chunk, / kFragTile
+    int32_t first;      // vec tiles: the gradient p; otherwise the first piece
     int32_t n_pieces;
-    int32_t j;          // chunk
-    int32_t vec;        // one aligned piece inside a gradient, n % 16 == 0
-    int32_t p;          // vec tiles: the gradient (so its pointers load with the tile)
-    int32_t pad;
+    uint16_t n;         // elements in the tile (<= kFragTile)
+    uint8_t j;          // chunk
+    uint8_t vec;        // one aligned piece inside a gradient, n % 16 == 0
 };
+static_assert(sizeof(FragTile) == 24, "packed tile record");
+static_assert(kFragTile <= 65535 && DPR_MAX_RANKS <= 255, "tile record field widths");
 
 struct FragPiece {
     int64_t tile_off;   // first element of the piece inside its tile
@@ -65,31 +78,37 @@ struct FragParams {
     int order;                  // kAfterPrevious / kBesidePrevious
 };
 
+// One tile of one bucket (the body of both kernels below).  `ptrs` is the
+// plan's [K * P] gradient table, `outs` the bucket's K fp32 shards, `base`
+// K shared-memory slots.  Everything before order_enter reads only the plan's
+// fixed tables.
 template <int KC, int MODE>
-__global__ void __launch_bounds__(kThreads) rs_fragments(const __grid_constant__ FragParams p) {
-    __shared__ const uint16_t* base[DPR_MAX_RANKS];
-    const FragTile tl = p.tiles[blockIdx.x];
-    const int K = KC > 0 ? KC : p.K;
+__device__ __forceinline__ void fragments_tile(const FragTile& tl, const FragPiece* pieces,
+                                               uint16_t* const* ptrs, int P, float* const* outs,
+                                               int K_rt, float scale, int accumulate,
+                                               int out_aligned32, int order,
+                                               const uint16_t** base) {
+    const int K = KC > 0 ? KC : K_rt;
     const int j = tl.j;
-    float* const out = p.out[j] + tl.t0;
-    if (tl.vec && p.out_aligned32) {
-        if (threadIdx.x < K) base[threadIdx.x] = p.ptrs[int64_t(threadIdx.x) * p.P + tl.p] + tl.src_off;
+    float* const out = outs[j] + int64_t(tl.t0_tiles) * kFragTile;
+    if (tl.vec && out_aligned32) {
+        if (threadIdx.x < K) base[threadIdx.x] = ptrs[int64_t(threadIdx.x) * P + tl.first] + tl.src_off;
         __syncthreads();
-        order_enter(p.order);           // the plan's tables above are fixed; the buffers are not
+        order_enter(order);             // the plan's tables above are fixed; the buffers are not
         for (int64_t u = threadIdx.x; u < tl.n / 16; u += kThreads) {
             float acc[16];
             ring_sum<KC, 1, MODE, 8, true>(base, K, j, uint64_t(16 * u), acc);
-            store_shard<8>(out + 16 * u, acc, p.scale, p.accumulate);
+            store_shard<8>(out + 16 * u, acc, scale, accumulate);
         }
-        order_exit(p.order);
+        order_exit(order);
         return;
     }
-    order_enter(p.order);
+    order_enter(order);
     for (int q = 0; q < tl.n_pieces; ++q) {
         __syncthreads();                       // the previous piece is done with base[]
-        const FragPiece pc = p.pieces[tl.piece0 + q];
+        const FragPiece pc = pieces[tl.first + q];
         if (threadIdx.x < K)
-            base[threadIdx.x] = pc.p >= 0 ? p.ptrs[int64_t(threadIdx.x) * p.P + pc.p] + pc.src_off
+            base[threadIdx.x] = pc.p >= 0 ? ptrs[int64_t(threadIdx.x) * P + pc.p] + pc.src_off
                                           : nullptr;
         __syncthreads();
         for (int64_t i = threadIdx.x; i < pc.len; i += kThreads) {
@@ -103,13 +122,80 @@ __global__ void __launch_bounds__(kThreads) rs_fragments(const __grid_constant__
                 else hop = (s == 0) ? x : add_bf16(hop, x);
             }
             if constexpr (MODE == DPR_SUM_HOP_BF16) acc = bf_1(hop);
-            float v = __fmul_rn(acc, p.scale);
+            float v = __fmul_rn(acc, scale);
             float* o = out + pc.tile_off + i;
-            if (p.accumulate) v = __fadd_rn(*o, v);
+            if (accumulate) v = __fadd_rn(*o, v);
             *o = v;
         }
     }
-    order_exit(p.order);
+    order_exit(order);
+}
+
+template <int KC, int MODE>
+__global__ void __launch_bounds__(kThreads, frag_min_blocks(KC)) rs_fragments(const __grid_constant__ FragParams p) {
+    __shared__ const uint16_t* base[DPR_MAX_RANKS];
+    order_start(p.order);
+    const FragTile tl = p.tiles[blockIdx.x];
+    fragments_tile<KC, MODE>(tl, p.pieces, p.ptrs, p.P, p.out, p.K, p.scale, p.accumulate,
+                             p.out_aligned32, p.order, base);
+}
+
+// Several buckets in one grid: the blocks of member m are
+// [tile0[m], tile0[m + 1]); each block finds its member by binary search over
+// tile0 (uniform across the block, in the parameter block) and runs the
+// member's tile.  Members share K, mode, scale and accumulate.
+constexpr int kMultiMembers = 128;     // members per launch
+constexpr int kMultiOuts = 2048;       // shard pointers per launch
+
+struct FragMember {
+    const FragTile* tiles;
+    const FragPiece* pieces;
+    uint16_t* const* ptrs;
+    int32_t P;
+    int32_t out0;           // the member's first shard pointer in out[]
+    int32_t out_aligned32;
+    int32_t pad;
+};
+
+struct FragMultiParams {
+    int64_t tile0[kMultiMembers + 1];
+    FragMember m[kMultiMembers];
+    float* out[kMultiOuts];
+    int n;
+    int K;
+    float scale;
+    int accumulate;
+    int order;
+};
+
+template <int KC, int MODE>
+__global__ void __launch_bounds__(kThreads, frag_min_blocks(KC)) rs_fragments_multi(const __grid_constant__ FragMultiParams p) {
+    __shared__ const uint16_t* base[DPR_MAX_RANKS];
+    order_start(p.order);
+    const int64_t b = blockIdx.x;
+    int lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.tile0[mid] <= b) lo = mid;
+        else hi = mid - 1;
+    }
+    const FragMember& mb = p.m[lo];
+    const FragTile tl = mb.tiles[b - p.tile0[lo]];
+    fragments_tile<KC, MODE>(tl, mb.pieces, mb.ptrs, mb.P, p.out + mb.out0, p.K, p.scale,
+                             p.accumulate, mb.out_aligned32, p.order, base);
+}
+
+template <int MODE>
+const void* rs_fragments_multi_for(int K) {
+    switch (K) {
+        case 2: return reinterpret_cast<const void*>(rs_fragments_multi<2, MODE>);
+        case 4: return reinterpret_cast<const void*>(rs_fragments_multi<4, MODE>);
+        case 8: return reinterpret_cast<const void*>(rs_fragments_multi<8, MODE>);
+        case 16: return reinterpret_cast<const void*>(rs_fragments_multi<16, MODE>);
+        case 32: return reinterpret_cast<const void*>(rs_fragments_multi<32, MODE>);
+        case 64: return reinterpret_cast<const void*>(rs_fragments_multi<64, MODE>);
+        default: return reinterpret_cast<const void*>(rs_fragments_multi<0, MODE>);
+    }
 }
 
 template <int MODE>
@@ -201,10 +287,10 @@ dpr_status dpr_fragments_plan_create(dpr_fragments_plan** plan, int K, int P, co
             const int64_t a = int64_t(j) * S + t0;
             const int64_t n = std::min(kFragTile, S - t0);
             FragTile tl;
-            tl.t0 = t0;
-            tl.n = n;
-            tl.j = j;
-            tl.piece0 = int32_t(pieces.size());
+            tl.t0_tiles = int32_t(t0 / kFragTile);
+            tl.n = uint16_t(n);
+            tl.j = uint8_t(j);
+            const int64_t piece0 = int64_t(pieces.size());
             while (g < order.size() && offset[order[g]] + numel[order[g]] <= a) ++g;
             int64_t at = a;
             for (size_t h = g; at < a + n; ++h) {
@@ -219,15 +305,18 @@ dpr_status dpr_fragments_plan_create(dpr_fragments_plan** plan, int K, int P, co
                 pieces.push_back(FragPiece{at - a, end - at, at - offset[p], p, 0});
                 at = end;
             }
-            tl.n_pieces = int32_t(pieces.size()) - tl.piece0;
-            const FragPiece& first = pieces[tl.piece0];
+            if (int64_t(pieces.size()) > int64_t(0x7FFFFFFF)) {
+                free_fragments_plan(pl);
+                return DPR_ERR_UNSUPPORTED;
+            }
+            tl.n_pieces = int32_t(int64_t(pieces.size()) - piece0);
+            const FragPiece& first = pieces[size_t(piece0)];
             bool vec = tl.n_pieces == 1 && first.p >= 0 && n % 16 == 0;
             for (int r = 0; r < K && vec; ++r)
                 vec = aligned(static_cast<const uint16_t*>(src[size_t(r) * P + first.p]) + first.src_off, 32);
             tl.vec = vec ? 1 : 0;
-            tl.p = vec ? first.p : -1;
+            tl.first = vec ? first.p : int32_t(piece0);
             tl.src_off = vec ? first.src_off : 0;
-            tl.pad = 0;
             pl->tiles.push_back(tl);
         }
     }
@@ -347,13 +436,47 @@ dpr_status dpr_reduce_scatter_fragments_batch(int n, const dpr_fragments_plan* c
     }
     // members are independent: no output touches another output or any source
     if (!pairwise_disjoint(outs) || any_overlap(outs, srcs)) return DPR_ERR_ALIAS;
+    // members with tiles, grouped into launches of one grid each: consecutive
+    // members with the same K, up to kMultiMembers members, kMultiOuts shard
+    // pointers and a 1-D grid's blocks per launch
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    bool first = true;
+    std::vector<FragMultiParams> launches;
+    size_t o_at = 0;
     for (int i = 0; i < n; ++i) {
+        const dpr_fragments_plan* pl = plans[i];
+        const size_t o_i = o_at;
+        o_at += size_t(pl->K);
         if (skip[i]) continue;
-        prm[i].order = first ? kAfterPrevious : kBesidePrevious;
-        first = false;
-        const cudaError_t e = launch_fragments(plans[i], prm[i], kern[i], s);
+        const int64_t t = int64_t(pl->tiles.size());
+        FragMultiParams* cur = launches.empty() ? nullptr : &launches.back();
+        if (!cur || cur->K != pl->K || cur->n == kMultiMembers ||
+            cur->m[cur->n - 1].out0 + 2 * pl->K > kMultiOuts ||
+            cur->tile0[cur->n] + t > int64_t(0x7FFFFFFF)) {
+            launches.emplace_back();
+            cur = &launches.back();
+            std::memset(cur, 0, sizeof(*cur));
+            cur->K = pl->K;
+            cur->scale = scale;
+            cur->accumulate = accumulate ? 1 : 0;
+        }
+        FragMember& mb = cur->m[cur->n];
+        mb.tiles = pl->d_tiles;
+        mb.pieces = pl->d_pieces;
+        mb.ptrs = pl->d_ptrs;
+        mb.P = pl->P;
+        mb.out0 = cur->n == 0 ? 0 : cur->m[cur->n - 1].out0 + cur->K;
+        mb.out_aligned32 = prm[i].out_aligned32;
+        for (int j = 0; j < pl->K; ++j) cur->out[mb.out0 + j] = out[o_i + j];
+        cur->tile0[cur->n + 1] = cur->tile0[cur->n] + t;
+        ++cur->n;
+    }
+    for (size_t l = 0; l < launches.size(); ++l) {
+        FragMultiParams& lp = launches[l];
+        lp.order = l == 0 ? kAfterPrevious : kBesidePrevious;
+        const void* k = (mode == DPR_SUM_RING_FP32) ? rs_fragments_multi_for<DPR_SUM_RING_FP32>(lp.K)
+                                                    : rs_fragments_multi_for<DPR_SUM_HOP_BF16>(lp.K);
+        void* args[] = {&lp};
+        const cudaError_t e = launch_kernel(k, dim3(unsigned(lp.tile0[lp.n])), args, s);
         if (e != cudaSuccess) return record_cuda_status(e);
     }
     return DPR_OK;

@@ -32,6 +32,7 @@ namespace {
 template <int KC, int M, int MODE, int W>
 __global__ void __launch_bounds__(kThreads) rs_vec(const __grid_constant__ RsParams p) {
     const int j = blockIdx.y;
+    order_start(p.order);
     order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < p.su;
          t += uint64_t(gridDim.x) * kThreads) {
@@ -67,6 +68,7 @@ template <int KC, int M, int MODE, int W>
 __global__ void __launch_bounds__(kThreads) rs_bf16_vec(const __grid_constant__ RsParams p) {
     const int j = blockIdx.y;
     uint16_t* const out = reinterpret_cast<uint16_t*>(p.out[j]);
+    order_start(p.order);
     order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < p.su;
          t += uint64_t(gridDim.x) * kThreads) {
@@ -83,6 +85,7 @@ __global__ void __launch_bounds__(kThreads) rs_bf16_scalar(const __grid_constant
     const int j = blockIdx.y, K = p.K, M = p.M;
     const uint64_t S = uint64_t(p.S), base = uint64_t(j) * S;
     uint16_t* const out = reinterpret_cast<uint16_t*>(p.out[j]);
+    order_start(p.order);
     order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < S;
          t += uint64_t(gridDim.x) * kThreads) {
@@ -135,6 +138,7 @@ __global__ void __launch_bounds__(kThreads) rs_scalar(const __grid_constant__ Rs
     const int j = blockIdx.y, K = p.K, M = p.M;
     const uint64_t S = uint64_t(p.S), base = uint64_t(j) * S;
     float* const out = p.out[j];
+    order_start(p.order);
     order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < S;
          t += uint64_t(gridDim.x) * kThreads) {

@@ -300,3 +300,35 @@ def test_fragments_batch_and_launch_switch(L):
     assert L.dpr_set_programmatic_launch(1, None) == OK
     assert L.dpr_set_programmatic_launch(1, ctypes.byref(prev)) == OK
     assert prev.value == 1
+
+
+def test_noalloc_records_a_failing_cuda_call():
+    """dpr_flatten_bucket_noalloc reports a failing CUDA call as DPR_ERR_CUDA
+    and keeps its code for dpr_last_cuda_error(), like every other entry
+    point.  Its first CUDA call is the capture-status query of the stream,
+    which fails on a machine without a GPU.  A source pointer is null, so on a
+    machine with a GPU the call is refused right after that query instead;
+    either way nothing is launched.  Run in a child process, so the recorded
+    error does not outlive the test."""
+    import subprocess
+    import sys
+    code = r"""
+import ctypes, sys
+sys.path.insert(0, %r)
+import gradient_reduction_gb300 as g
+L = g.lib()
+src = (ctypes.c_void_p * 2)(0x7F0000000000, 0)
+dst = (ctypes.c_void_p * 2)(0x7F0000100000, 0x7F0000200000)
+n = (ctypes.c_int64 * 1)(16)
+o = (ctypes.c_int64 * 1)(0)
+st = L.dpr_flatten_bucket_noalloc(2, 1, src, n, o, 16, dst, None)
+print(st, L.dpr_last_cuda_error())
+""" % ROOT
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    st, err = map(int, out.stdout.split())
+    assert st in (CUDA, INVALID)
+    if st == CUDA:
+        assert err != 0
+    else:
+        assert err == 0

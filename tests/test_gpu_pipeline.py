@@ -245,7 +245,7 @@ def test_refused_submits_enqueue_nothing():
     serial = _serial(K, buckets, plans, dev)
     cur = torch.cuda.Stream()
     outs = [[torch.full((b.numel // K,), 7.0, device=dev) for _ in range(K)] for b in buckets]
-    spare = torch.full((buckets[0].numel // K + 1,), 5.0, device=dev)
+    spare = torch.full((buckets[1].numel // K + 1,), 5.0, device=dev)
     producers = [torch.cuda.Stream() for _ in range(9)]
     with dpr.BucketPipeline(K, max(b.numel for b in buckets), 2) as pipe:
         for bi, (plan, o) in enumerate(zip(plans, outs)):

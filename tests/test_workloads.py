@@ -68,3 +68,43 @@ def test_index_evaluation_matches_ranges():
         assert np.array_equal(_bits(cfg.at(1, 0, idx)), full[idx])
     u = _bits(C.cfg4_slab(0, 123_457))
     assert np.array_equal(_bits(C.cfg4_at(idx)), u[idx])
+
+
+def test_series_logarithm_matches_libm():
+    """The generator's own ln(u1) (exact split, atanh series) is within 2 ulp
+    of the C library's log over a spread of words, the ends included."""
+    w = torch.arange(0, 1 << 18, dtype=torch.int64) * 16381 % (1 << 32)
+    w = torch.cat([w, torch.tensor([0, 1, 2, 3, 4, (1 << 31) - 1, 1 << 31, 3037000499,
+                                    (1 << 32) - 2, (1 << 32) - 1])])
+    got = syn._ln_u1(w).numpy()
+    want = np.log((w.numpy().astype(np.float64) + 1.0) * 2.0 ** -32)
+    nz = want != 0
+    assert got[~nz].tolist() == [0.0]                       # u1 = 1
+    ulps = np.abs(got - want)[nz] / np.spacing(np.abs(want[nz]))
+    assert ulps.max() <= 2.0
+
+
+def test_series_cosine_matches_libm():
+    """cos(2 pi u2) by exact octant reduction and Taylor polynomials agrees
+    with the C library's cos to 1e-15 absolute, including every octant edge."""
+    edges = [o << 29 for o in range(8)]
+    edges += [e + d for e in edges for d in (-1, 1) if 0 <= e + d < (1 << 32)]
+    w = torch.cat([torch.arange(0, 1 << 18, dtype=torch.int64) * 16411 % (1 << 32),
+                   torch.tensor(edges + [(1 << 32) - 1], dtype=torch.int64)])
+    got = syn._cos_2pi_u2(w).numpy()
+    want = np.cos(2.0 * np.pi * (w.numpy().astype(np.float64) * 2.0 ** -32))
+    assert np.abs(got - want).max() < 1e-15
+    assert got[w.numpy() == 0][0] == 1.0
+
+
+def test_gauss_is_a_normal_sample():
+    """Box-Muller values: Kolmogorov-Smirnov against N(0, 1) (the bf16 grid is
+    far finer than the test's resolution at this sample size), the first two
+    moments, and the 6.66-sigma cut of the tails."""
+    from scipy import stats
+    x = syn.gauss_bf16(0, 1 << 18, syn.stream_key(5, 1), 1.0).double().numpy()
+    assert stats.kstest(x, "norm").pvalue > 1e-3
+    assert abs(x.mean()) < 0.01 and abs(x.std() - 1.0) < 0.01
+    assert np.abs(x).max() <= 6.67
+    y = syn.gauss_bf16(0, 1 << 16, syn.stream_key(5, 2), 1e-3).double().numpy()
+    assert abs(y.std() - 1e-3) < 2e-5

@@ -7,8 +7,7 @@ device.  It keeps its segment table in a fixed array inside the library.
 These tests call it through the C ABI and compare its output, bit for bit,
 with the plan-based gather (dpr_flatten_plan_create + dpr_flatten_bucket) and
 with the oracle's gather on two calls in a row; check that a call beyond the
-fixed table is refused, that a failing call leaves its CUDA error for
-dpr_last_cuda_error(), and that a call on a capturing stream is refused
+fixed table is refused, and that a call on a capturing stream is refused
 without breaking the capture.  The file's name sorts it last, so a failure
 here cannot stop a run that halts at the first failure before the other GPU
 tests have run; it also passes on its own in a fresh process."""
@@ -133,28 +132,3 @@ def test_noalloc_is_refused_on_a_capturing_stream_and_the_capture_survives():
     torch.cuda.synchronize()
     assert float(x[0]) == 2.0
     assert all(int(t.view(torch.int16).abs().sum()) == 0 for t in dst)   # nothing was written
-
-
-def test_noalloc_records_its_cuda_error():
-    """A failing CUDA call inside the entry point is reported as DPR_ERR_CUDA
-    with its code kept for dpr_last_cuda_error(), like every other call.  The
-    failure is made on the host: while another stream captures in global
-    mode, asking whether the legacy default stream is capturing fails with
-    cudaErrorStreamCaptureImplicit, before anything is enqueued."""
-    dev = H.device()
-    L = dpr.lib()
-    srcs, offsets, bucket = _case(2, [64, 32], 3, dev)
-    dst = [torch.zeros(bucket, dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    x = torch.ones(16, device=dev)
-    g = torch.cuda.CUDAGraph()
-    st = code = None
-    try:
-        with torch.cuda.graph(g, capture_error_mode="global"):
-            st = _call_noalloc_raw(L, srcs, [64, 32], offsets, bucket, dst, 0)
-            code = L.dpr_last_cuda_error()
-            x.add_(1.0)
-    except RuntimeError:
-        pass            # the capture's fate is not what this test checks
-    torch.cuda.synchronize()
-    assert st == 4, st
-    assert code == 906, code          # cudaErrorStreamCaptureImplicit

@@ -10,14 +10,27 @@ so any element range of any rank buffer can be regenerated on its own
 same slab generated on a GPU.  Bit-identity holds because the recipe uses only
   * 64-bit integer arithmetic whose intermediates never exceed 2**63
     (32-bit multiplies are split into 16-bit halves),
-  * one exact int -> fp32 conversion (|z| < 2**24),
-  * one or two IEEE fp32 multiplies (correctly rounded on every device), and
-  * PyTorch's fp32 -> bf16 conversion, round-to-nearest-even on CPU and CUDA.
+  * exact integer -> float conversions and exact bit manipulations,
+  * IEEE double and fp32 additions, multiplications, tensor-by-tensor
+    divisions and square roots, each a separate, correctly rounded operation
+    on every device (no fused multiply-add, no library transcendental), and
+  * PyTorch's fp64 -> fp32 and fp32 -> bf16 conversions, round-to-nearest-even
+    on CPU and CUDA.
 
 Distributions
-  gauss:   centred Irwin-Hall sum of four 16-bit uniforms, scaled to standard
-           deviation sigma (a bounded, bell-shaped stand-in for N(0, sigma));
-           optionally a fraction of the entries multiplied by an outlier factor.
+  gauss:   N(0, sigma) by the Box-Muller transform (Box and Muller, 1958) in
+           IEEE double precision: two 32-bit hash words give u1 in (0, 1] and
+           u2 in [0, 1), and z = sqrt(-2 ln u1) cos(2 pi u2).  ln and cos are
+           evaluated here by series (ln m = 2 atanh((m-1)/(m+1)) after an
+           exact split u1 = m 2^e; cos by octant reduction done exactly on the
+           integer word and Taylor polynomials on [0, pi/4]) using only
+           additions, multiplications, one tensor-by-tensor division and one
+           square root, each correctly rounded on every device, so a host slab
+           and a GPU slab are bit-identical.  |z| <= sqrt(64 ln 2) = 6.66, so
+           the tails beyond 6.66 sigma (probability 3e-11) are cut.  x = sigma z
+           is rounded to fp32, optionally a fraction of the entries is
+           multiplied by an outlier factor in fp32, and the result is rounded
+           to bf16.
   uniform: 24-bit uniform integer scaled onto [-amp, amp).
   integer: small integer-valued buffers for worked examples.
 
@@ -94,9 +107,64 @@ def _words_at(idx: torch.Tensor, key: int) -> tuple:
     return _fmix32(base ^ _W0), _fmix32(base ^ _W1), _fmix32(base ^ _W2)
 
 
-# standard deviation of the sum of four independent uniforms on {0..65535}
-_IRWIN_HALL4_STD = math.sqrt(4.0 * (65536.0 ** 2 - 1.0) / 12.0)
-_IRWIN_HALL4_MEAN = 2 * 65535
+_LN2 = math.log(2.0)
+_PI_4 = math.pi / 4.0
+_SQRT2 = math.sqrt(2.0)
+# ln m = 2 (z + z^3/3 + z^5/5 + ...), z = (m-1)/(m+1), |z| <= 0.1716 on
+# [1/sqrt2, sqrt2]: 12 terms leave a truncation below 2^-60
+_ATANH_C = [1.0 / (2 * k + 1) for k in range(12)]
+# Taylor coefficients of sin(x)/x and cos(x) in x^2, to x^18 / x^20: on
+# [0, pi/4] the first omitted term is below 2^-65
+_SIN_C = [(-1.0) ** k / math.factorial(2 * k + 1) for k in range(10)]
+_COS_C = [(-1.0) ** k / math.factorial(2 * k) for k in range(11)]
+
+
+def _horner(c, x2):
+    """sum_k c[k] x2^k by Horner's rule: one multiply and one add per step."""
+    acc = torch.full_like(x2, c[-1])
+    for ck in reversed(c[:-1]):
+        acc = acc * x2 + ck
+    return acc
+
+
+def _ln_u1(w0: torch.Tensor) -> torch.Tensor:
+    """ln(u1) in double, u1 = (w0 + 1) 2^-32 in (0, 1], for int64 words w0 in
+    [0, 2^32).  n = w0 + 1 is split exactly as n = m 2^e with m in
+    [1/sqrt2, sqrt2) (from its double's exponent and mantissa bits), and
+    ln u1 = (e - 32) ln 2 + 2 atanh((m-1)/(m+1))."""
+    d = (w0 + 1).to(torch.float64)                    # exact: n <= 2^32
+    b = d.view(torch.int64)
+    e = (b >> 52) - 1023
+    m = ((b & ((1 << 52) - 1)) | (1023 << 52)).view(torch.float64)   # [1, 2)
+    big = m > _SQRT2
+    m = torch.where(big, m * 0.5, m)                  # exact
+    e = e + big.to(torch.int64)
+    z = (m - 1.0) / (m + 1.0)
+    z2 = z * z
+    ln_m = (z * _horner(_ATANH_C, z2)) * 2.0
+    return (e - 32).to(torch.float64) * _LN2 + ln_m
+
+
+def _cos_2pi_u2(w1: torch.Tensor) -> torch.Tensor:
+    """cos(2 pi u2) in double, u2 = w1 2^-32 in [0, 1), for int64 words w1 in
+    [0, 2^32).  The octant o = w1 >> 29 and the fraction f in [0, 1) inside it
+    are exact; theta = k pi/2 + s psi with psi in [0, pi/4]:
+      even o: k = o/2,       s = +1, psi = f pi/4;
+      odd o:  k = (o+1)/2,   s = -1, psi = (1 - f) pi/4;
+    cos(k pi/2 + s psi) is cos psi, -s sin psi, -cos psi, s sin psi for
+    k mod 4 = 0, 1, 2, 3."""
+    o = w1 >> 29
+    f = (w1 & ((1 << 29) - 1)).to(torch.float64) * (2.0 ** -29)     # exact
+    odd = (o & 1) == 1
+    psi = torch.where(odd, 1.0 - f, f) * _PI_4
+    x2 = psi * psi
+    sin_p = psi * _horner(_SIN_C, x2)
+    cos_p = _horner(_COS_C, x2)
+    k = ((o + 1) >> 1) & 3
+    s = torch.where(odd, -1.0, 1.0).to(torch.float64)
+    val = torch.where((k & 1) == 1, sin_p, cos_p)
+    sign = torch.where(k == 0, 1.0, torch.where(k == 2, -1.0, torch.where(k == 1, -s, s)))
+    return val * sign
 
 
 def gauss_bf16(start: int, count: int, key: int, sigma: float,
@@ -114,10 +182,8 @@ def gauss_bf16(start: int, count: int, key: int, sigma: float,
 
 
 def _gauss_from_words(w0, w1, w2, sigma, outlier_frac, outlier_mult, device):
-    scale = torch.tensor(float(np.float32(sigma / _IRWIN_HALL4_STD)), dtype=torch.float32,
-                         device=device)
-    z = (w0 & 0xFFFF) + (w0 >> 16) + (w1 & 0xFFFF) + (w1 >> 16) - _IRWIN_HALL4_MEAN
-    x = z.to(torch.float32) * scale
+    r = torch.sqrt(_ln_u1(w0) * -2.0)
+    x = ((r * _cos_2pi_u2(w1)) * float(sigma)).to(torch.float32)
     thresh = int(outlier_frac * 4294967296.0)
     if thresh > 0:
         mult = torch.tensor(float(np.float32(outlier_mult)), dtype=torch.float32, device=device)
