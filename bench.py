@@ -59,25 +59,38 @@ STEP_KERNELS = ("flatten", "rs_fp32_m2", "rs_hop_m2_acc", "allgather", "allreduc
 Z3_KERNELS = ("rs_coalesced", "ag_coalesced")
 BF16_KERNELS = ("rs_bf16_copy", "rs_bf16_add", "cast")
 
-# DRAM traffic per launch from one ncu capture of each kernel (read + write
-# bytes at the bench's launch size), valid only while the kernel's sources
-# hash to `src_sha`; otherwise reported as null.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per full-size
+# launch, scaled from one ncu capture of a small case of the same kernel: the
+# bench's step kernels at 2**25 elements per rank (x16 to the full 2**29), the
+# per-parameter kernels on one layer of the 7-layer model (x7), the bf16
+# partition kernels at 2**25 elements per rank (x16).  Each entry holds only
+# while the kernel's sources hash to `src_sha`; otherwise the bench reports
+# null.  Dirty lines still in L2 when a kernel ends (at most the L2's 129 MB)
+# are not counted at either size, so the scaled write traffic is a slight
+# underestimate.
 NCU_TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum at the bench's full size
-    # (K=8, N=2**29), one launch each (profiles/step_k8_1GiB_dram_traffic.md); src_sha is
-    # kernel_src_sha(kernel) of the sources the capture was taken from
-    "flatten": {"bytes": 17_129_000_000, "src_sha": "37b74f39084a227f"},
-    "rs_fp32_m2": {"bytes": 19_312_000_000, "src_sha": "7aab38c883045de4"},
-    "rs_hop_m2_acc": {"bytes": 21_460_000_000, "src_sha": "7aab38c883045de4"},
-    "allgather": {"bytes": 9_600_000_000, "src_sha": "37b74f39084a227f"},
-    "allreduce": {"bytes": 17_121_000_000, "src_sha": "7aab38c883045de4"},
-    # the same metrics on the other workloads' first timed step
-    # (profiles/zero3_and_bf16_partition_dram_traffic.md)
-    "rs_coalesced": {"bytes": 22_005_000_000, "src_sha": "410864765ad8f3d1"},
-    "ag_coalesced": {"bytes": 19_756_000_000, "src_sha": "ba2c21a57ae06ff6"},
-    "rs_bf16_copy": {"bytes": 9_654_000_000, "src_sha": "7aab38c883045de4"},
-    "rs_bf16_add": {"bytes": 10_725_000_000, "src_sha": "7aab38c883045de4"},
-    "cast": {"bytes": 3_163_000_000, "src_sha": "70432212ab8c1e1f"},
+    "flatten": {"bytes": 16_313_106_432, "small_case_bytes": 1_019_569_152, "scale": 16,
+        "src_sha": "6474650912caab0c"},
+    "rs_fp32_m2": {"bytes": 19_156_946_944, "small_case_bytes": 1_197_309_184, "scale": 16,
+        "src_sha": "4675ad59026b5fb6"},
+    "rs_hop_m2_acc": {"bytes": 21_306_318_848, "small_case_bytes": 1_331_644_928, "scale": 16,
+        "src_sha": "4675ad59026b5fb6"},
+    "allgather": {"bytes": 8_733_552_640, "small_case_bytes": 545_847_040, "scale": 16,
+        "src_sha": "6474650912caab0c"},
+    "allreduce": {"bytes": 16_274_710_528, "small_case_bytes": 1_017_169_408, "scale": 16,
+        "src_sha": "4675ad59026b5fb6"},
+    "rs_fp32_m1": {"bytes": 10_438_463_488, "small_case_bytes": 652_403_968, "scale": 16,
+        "src_sha": "4675ad59026b5fb6"},
+    "rs_coalesced": {"bytes": 21_884_484_608, "small_case_bytes": 3_126_354_944, "scale": 7,
+        "src_sha": "7951d2db94cd0679"},
+    "ag_coalesced": {"bytes": 19_396_910_848, "small_case_bytes": 2_770_987_264, "scale": 7,
+        "src_sha": "05f53611035fac79"},
+    "rs_bf16_copy": {"bytes": 9_514_078_208, "small_case_bytes": 594_629_888, "scale": 16,
+        "src_sha": "4675ad59026b5fb6"},
+    "rs_bf16_add": {"bytes": 10_587_287_552, "small_case_bytes": 661_705_472, "scale": 16,
+        "src_sha": "4675ad59026b5fb6"},
+    "cast": {"bytes": 2_336_284_672, "small_case_bytes": 146_017_792, "scale": 16,
+        "src_sha": "d72896eb3f85bb94"},
 }
 
 
@@ -121,7 +134,8 @@ def parse_args(argv=None):
                         "its bench line is quoted only at the default 7")
     p.add_argument("--bucket-elems", type=int, default=25_000_000,
                    help="configs: bucket cap of configuration 3, in elements per rank")
-    p.add_argument("--only", choices=STEP_KERNELS + Z3_KERNELS + BF16_KERNELS, default=None,
+    p.add_argument("--only", choices=STEP_KERNELS + ("rs_fp32_m1", "rs_hop_m1") + Z3_KERNELS
+                   + BF16_KERNELS, default=None,
                    help="profile helper: launch only this kernel per step")
     p.add_argument("--graph", action="store_true",
                    help="capture one step's launches in a CUDA graph and replay it")
@@ -232,6 +246,8 @@ KERNEL_SOURCES = {
     "rs_fp32_m2": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
     "rs_hop_m2_acc": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
     "allreduce": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
+    "rs_fp32_m1": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
+    "rs_hop_m1": ["reduce_kernels.cu", "dpr_ring.cuh"] + _COMMON_SRC,
     "rs_coalesced": ["coalesced.cu", "dpr_ring.cuh", "dpr_device.cuh", "dpr_kernels.h",
                      "host_checks.h"],
     "ag_coalesced": ["coalesced.cu", "dpr_device.cuh", "dpr_kernels.h", "host_checks.h"],
@@ -367,6 +383,8 @@ class Workload:
             "rs_hop_m2_acc": 2 * 2 * K * N + 4 * N + 4 * N,
             "allgather": 2 * N + 2 * K * N,
             "allreduce": 4 * K * N,
+            "rs_fp32_m1": 2 * K * N + 4 * N,
+            "rs_hop_m1": 2 * K * N + 4 * N,
         }
         self.launches_per_step = len(STEP_KERNELS)
 
@@ -392,6 +410,12 @@ class Workload:
         elif name == "allreduce":
             dpr.dpr_allreduce(self.ipg1, K, N, self.ar_out, mode=dpr.RING_FP32, scale=1.0 / K,
                               stream=s)
+        elif name == "rs_fp32_m1":          # the metric's own reduce-scatter (profile helper)
+            dpr.dpr_reduce_scatter(self.ipg0, K, 1, N, self.part_f32, mode=dpr.RING_FP32,
+                                   scale=1.0 / K, stream=s)
+        elif name == "rs_hop_m1":
+            dpr.dpr_reduce_scatter(self.ipg0, K, 1, N, self.part_f32, mode=dpr.HOP_BF16,
+                                   scale=1.0 / K, stream=s)
         else:
             raise ValueError(name)
 
@@ -467,13 +491,15 @@ class Bf16PartitionWorkload:
     casts the partition to fp32."""
     kernels = ("rs_bf16_copy", "rs_bf16_add", "cast")
 
-    def __init__(self, dev, stream):
+    def __init__(self, dev, stream, n_per_rank=None):
         import torch
         import gradient_reduction_gb300 as dpr
         from workloads import configs as C
         self.dpr, self.torch, self.dev, self.stream = dpr, torch, dev, stream
         w = C.BENCH
-        K, N = w.K, w.N
+        K, N = w.K, (n_per_rank or w.N)
+        if N % (16 * K):
+            raise ValueError("--n-per-rank must be a multiple of 16 K")
         S = N // K
         with torch.cuda.stream(stream):
             self.x = torch.empty(2, K, N, dtype=torch.bfloat16, device=dev)
@@ -815,7 +841,7 @@ def run_fragments_bench(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     s = torch.cuda.Stream(device=dev)
-    wl = Workload(dev, s)
+    wl = Workload(dev, s, args.n_per_rank)
     K, N, P, F = wl.K, wl.N, wl.P, wl.F
     S = N // K
     timed = LaunchTimer(s, args.steps, args.warmup)
@@ -1038,7 +1064,8 @@ def run_point_bench(args):
 
 def run_sweep_bench(args):
     """Configuration 5's sweep: effective GB/s of the reduce-scatter (both
-    modes, 2 micro-batches), all-gather and all-reduce for K in
+    modes, 2 micro-batches, and 1 micro-batch beside them), all-gather and
+    all-reduce for K in
     {2,4,8,16,64} and 1 KiB .. 1 GiB per rank.  Each figure is algorithmic
     bytes over the average launch time (CUDA events); small sizes show the
     launch-bound regime."""
@@ -1056,7 +1083,10 @@ def run_sweep_bench(args):
         N = nbytes // 2
         S = N // K
         row = {"K": K, "bytes_per_rank": nbytes}
-        x = torch.empty(2 * K, N, dtype=torch.bfloat16, device=dev).normal_()
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(C.BASE_SEED + 5)            # N(0, 1e-3), seeded, drawn on the device
+        x = torch.empty(2 * K, N, dtype=torch.bfloat16, device=dev).normal_(0.0, 1e-3,
+                                                                             generator=gen)
         xs = list(x.unbind(0))
         out = torch.empty(K, S, dtype=torch.float32, device=dev)
         outs = list(out.unbind(0))
@@ -1064,9 +1094,13 @@ def run_sweep_bench(args):
             t = timed(lambda: dpr.dpr_reduce_scatter(xs, K, 2, N, outs, mode=mode, stream=s),
                       4 * K * N + 4 * N)
             row[name] = round((4 * K * N + 4 * N) / t / 1e9, 1)
+        for mode, name in ((dpr.RING_FP32, "rs_fp32_m1"), (dpr.HOP_BF16, "rs_hop_m1")):
+            t = timed(lambda: dpr.dpr_reduce_scatter(xs[:K], K, 1, N, outs, mode=mode, stream=s),
+                      2 * K * N + 4 * N)
+            row[name] = round((2 * K * N + 4 * N) / t / 1e9, 1)
         del xs, x, out, outs
         torch.cuda.empty_cache()
-        x = torch.empty(K, N, dtype=torch.bfloat16, device=dev).normal_()
+        x = torch.empty(K, N, dtype=torch.bfloat16, device=dev).normal_(0.0, 1e-3, generator=gen)
         y = torch.empty(K, N, dtype=torch.bfloat16, device=dev)
         xs, ys = list(x.unbind(0)), list(y.unbind(0))
         t = timed(lambda: dpr.dpr_allreduce(xs, K, N, ys, stream=s), 4 * K * N)
@@ -1144,7 +1178,7 @@ def run_device(args, rank, world, local_rank):
         wl = Zero3Workload(dev, stream, args.z3_layers)
         kernels = (args.only,) if args.only else Z3_KERNELS
     elif args.workload == "bf16_partition":
-        wl = Bf16PartitionWorkload(dev, stream)
+        wl = Bf16PartitionWorkload(dev, stream, args.n_per_rank)
         kernels = (args.only,) if args.only else BF16_KERNELS
     else:
         wl = Workload(dev, stream, args.n_per_rank)
@@ -1228,15 +1262,15 @@ def time_headline_ops(wl, launches: int, warmup: int):
     ops = {
         "rs_ring_fp32_m1": (lambda: dpr.dpr_reduce_scatter(wl.ipg0, K, 1, N, wl.part_f32,
                                                            mode=dpr.RING_FP32, stream=s),
-                            2 * K * N + 4 * N),
+                            2 * K * N + 4 * N, "rs_fp32_m1"),
         "rs_hop_bf16_m1": (lambda: dpr.dpr_reduce_scatter(wl.ipg0, K, 1, N, wl.part_f32,
                                                           mode=dpr.HOP_BF16, stream=s),
-                           2 * K * N + 4 * N),
+                           2 * K * N + 4 * N, "rs_hop_m1"),
         "allgather": (lambda: dpr.dpr_allgather(wl.shards, K, N, wl.params, stream=s),
-                      2 * N + 2 * K * N),
+                      2 * N + 2 * K * N, "allgather"),
     }
     out = {}
-    for name, (fn, nbytes) in ops.items():
+    for name, (fn, nbytes, key) in ops.items():
         for _ in range(warmup):
             fn()
         s.synchronize()
@@ -1249,10 +1283,13 @@ def time_headline_ops(wl, launches: int, warmup: int):
         s.synchronize()
         t = a.elapsed_time(b) / 1e3 / launches
         gbs = nbytes / t / 1e9
+        tr = NCU_TRAFFIC.get(key)
         out[name] = {"bytes_per_launch": nbytes, "avg_ms": round(t * 1e3, 4),
                      "launches": launches, "gbs": round(gbs, 1),
                      "frac_of_measured_peak": round(gbs / peak, 4),
-                     "frac_of_nominal_peak": round(gbs / NOMINAL_HBM_GBS, 4)}
+                     "frac_of_nominal_peak": round(gbs / NOMINAL_HBM_GBS, 4),
+                     "traffic": tr["bytes"] if tr and tr["src_sha"] == kernel_src_sha(key)
+                     and wl.N == 1 << 29 else None}
     out["peaks"] = {"measured_gbs": peak, "measured_kind": kind,
                     "nominal_gbs": NOMINAL_HBM_GBS,
                     "nominal_is": "GB300 HBM3e data-sheet bandwidth"}
@@ -1596,7 +1633,8 @@ def main(argv=None):
     d = kern[dom]
     sha = kernel_src_sha()
     tr = NCU_TRAFFIC.get(dom)
-    traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_sha(dom) else None
+    traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_src_sha(dom) \
+        and not args.n_per_rank and not args.z3_layers else None
     value = job_value(res["step_bytes"], args.steps, world, res["max_elapsed"])
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -1642,7 +1680,8 @@ def main(argv=None):
                           "l2": "inputs (42 GB resident) far larger than L2; no flush needed"}
         line["e2e"] = None
     if args.workload == "bf16_partition":
-        line["config"] = {"workload": "zero3_bf16_partition_k8_1GiB", "K": 8,
+        line["config"] = {"workload": "zero3_bf16_partition_k8_1GiB" if not args.n_per_rank
+                          else f"zero3_bf16_partition_k8_profile_case_{res['wl'].N}", "K": 8,
                           "elements_per_rank": res["wl"].N,
                           "step": "RS into bf16 partitions (copy_) + RS with bf16 add_ + "
                                   "step-time cast to fp32",

@@ -33,12 +33,12 @@ namespace {
 #define DPR_FRAG_TILE 4096
 #endif
 constexpr int64_t kFragTile = DPR_FRAG_TILE;     // elements per chunk tile, one block each
-// Blocks per SM the fragments kernels are compiled for, for K <= 8: 5 caps
-// them at 48 registers, one block more per SM than their natural 54-56,
-// which hides the per-block table reads that come before the first data
-// load.  Larger K keeps the compiler's choice (a cap would spill).
+// Minimum blocks per SM the fragments kernels are compiled for, for K <= 8
+// (larger K keeps the compiler's choice, which a cap would make spill).  1
+// leaves the register count to the compiler: with the packed tile record and
+// its L2 prefetch, a cap of 48 registers (5 blocks per SM) measured slower.
 #ifndef DPR_FRAG_MIN_BLOCKS
-#define DPR_FRAG_MIN_BLOCKS 5
+#define DPR_FRAG_MIN_BLOCKS 1
 #endif
 constexpr int frag_min_blocks(int KC) { return (KC > 0 && KC <= 8) ? DPR_FRAG_MIN_BLOCKS : 1; }
 
@@ -66,6 +66,7 @@ struct FragPiece {
 
 struct FragParams {
     const FragTile* tiles;
+    int64_t n_tiles;
     const FragPiece* pieces;
     uint16_t* const* ptrs;      // device table [K * P]: src[r * P + p]
     float* out[DPR_MAX_RANKS];
@@ -131,10 +132,24 @@ __device__ __forceinline__ void fragments_tile(const FragTile& tl, const FragPie
     order_exit(order);
 }
 
+// Blocks ahead whose tile record a block asks L2 to fetch (a little more
+// than one wave of resident blocks), so that the record a block reads first
+// is an L2 hit rather than a DRAM miss.
+#ifndef DPR_FRAG_PREFETCH_AHEAD
+#define DPR_FRAG_PREFETCH_AHEAD 1024
+#endif
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 template <int KC, int MODE>
 __global__ void __launch_bounds__(kThreads, frag_min_blocks(KC)) rs_fragments(const __grid_constant__ FragParams p) {
     __shared__ const uint16_t* base[DPR_MAX_RANKS];
     order_start(p.order);
+    if (DPR_FRAG_PREFETCH_AHEAD > 0 && threadIdx.x == 0 &&
+        int64_t(blockIdx.x) + DPR_FRAG_PREFETCH_AHEAD < p.n_tiles)
+        prefetch_l2(p.tiles + blockIdx.x + DPR_FRAG_PREFETCH_AHEAD);
     const FragTile tl = p.tiles[blockIdx.x];
     fragments_tile<KC, MODE>(tl, p.pieces, p.ptrs, p.P, p.out, p.K, p.scale, p.accumulate,
                              p.out_aligned32, p.order, base);
@@ -180,6 +195,9 @@ __global__ void __launch_bounds__(kThreads, frag_min_blocks(KC)) rs_fragments_mu
         else hi = mid - 1;
     }
     const FragMember& mb = p.m[lo];
+    if (DPR_FRAG_PREFETCH_AHEAD > 0 && threadIdx.x == 0 &&
+        b + DPR_FRAG_PREFETCH_AHEAD < p.tile0[lo + 1])
+        prefetch_l2(mb.tiles + (b - p.tile0[lo]) + DPR_FRAG_PREFETCH_AHEAD);
     const FragTile tl = mb.tiles[b - p.tile0[lo]];
     fragments_tile<KC, MODE>(tl, mb.pieces, mb.ptrs, mb.P, p.out + mb.out0, p.K, p.scale,
                              p.accumulate, mb.out_aligned32, p.order, base);
@@ -376,6 +394,7 @@ dpr_status prepare_fragments(const dpr_fragments_plan* plan, float* const* out, 
     *empty = plan->tiles.empty();
     std::memset(prm, 0, sizeof(*prm));
     prm->tiles = plan->d_tiles;
+    prm->n_tiles = int64_t(plan->tiles.size());
     prm->pieces = plan->d_pieces;
     prm->ptrs = plan->d_ptrs;
     for (int j = 0; j < K; ++j) prm->out[j] = out[j];
