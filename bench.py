@@ -903,12 +903,15 @@ def run_sequence_bench(args):
             syn.gauss_bf16(0, N, syn.stream_key(args.seed, i % K, i // K), 1e-3, device=dev,
                            out=x[0, i])
         x[1:].copy_(x[0].expand(nb - 1, M * K, N))
-        ins = [list(x[b].unbind(0)) for b in range(nb)]
+        ins = [x[b] for b in range(nb)]              # one [M*K, N] tensor per bucket
         outs = {k: torch.empty(nb, K, S, dtype=f32, device=dev) for k in ("plain", "pdl", "batch")}
-        out_l = {k: [list(v[b].unbind(0)) for b in range(nb)] for k, v in outs.items()}
+        out_l = {k: [v[b] for b in range(nb)] for k, v in outs.items()}   # [K, S] per bucket
+        ins_list = [list(x[b].unbind(0)) for b in range(nb)]              # the list form
+        outs_list = [list(outs["plain"][b].unbind(0)) for b in range(nb)]
         full = torch.empty(nb, K, N, dtype=bf, device=dev)
-        full_l = [list(full[b].unbind(0)) for b in range(nb)]
-        shards = [[x[b, j, j * S:(j + 1) * S] for j in range(K)] for b in range(nb)]
+        full_l = [full[b] for b in range(nb)]
+        # shard j of bucket b is chunk j of rank j's buffer: rows N + S elements apart
+        shards = [torch.as_strided(x[b], (K, S), (N + S, 1)) for b in range(nb)]
     s.synchronize()
 
     def rs_single(key):
@@ -916,8 +919,17 @@ def run_sequence_bench(args):
             dpr.dpr_reduce_scatter(ins[b], K, M, N, out_l[key][b], mode=dpr.RING_FP32, stream=s)
 
     def rs_batch():
-        dpr.dpr_reduce_scatter_batch(ins, K, M, [N] * nb, out_l["batch"], mode=dpr.RING_FP32,
+        dpr.dpr_reduce_scatter_batch(x, K, M, [N] * nb, outs["batch"], mode=dpr.RING_FP32,
                                      stream=s)
+
+    def host_us(fn, calls):
+        """Host time per call of fn (no synchronisation inside the loop)."""
+        s.synchronize()
+        t0 = time.perf_counter()
+        fn()
+        t1 = time.perf_counter()
+        s.synchronize()
+        return (t1 - t0) / calls * 1e6
 
     def ag_single():
         for b in range(nb):
@@ -980,6 +992,15 @@ def run_sequence_bench(args):
     dpr.dpr_set_programmatic_launch(prev)
     same = all(torch.equal(outs["plain"].view(torch.int32), outs[k].view(torch.int32))
                for k in ("pdl", "batch"))
+    # the binding's host cost per call, with rank buffers passed as lists of tensors and
+    # as one stacked tensor per bucket
+    host = {
+        "list_args_us_per_call": round(host_us(lambda: [
+            dpr.dpr_reduce_scatter(ins_list[b], K, M, N, outs_list[b], stream=s)
+            for b in range(nb)], nb), 2),
+        "stacked_args_us_per_call": round(host_us(lambda: rs_single("plain"), nb), 2),
+        "batched_call_us_per_bucket": round(host_us(rs_batch, nb), 2),
+    }
     peak, kind = load_peaks()
 
     def fig(nbytes, t):
@@ -1006,9 +1027,10 @@ def run_sequence_bench(args):
                           "graph_plain_launches": fig(ag_bytes, t_ag_plain_g),
                           "graph_programmatic_launches": fig(ag_bytes, t_ag_pdl_g),
                           "bytes": ag_bytes},
+            "host_cost": host,
             "host_note": "eager rows include the Python binding's per-call cost (one call per "
-                         "bucket, except the batched call); graph rows replay the same launches "
-                         "from a CUDA graph"}
+                         "bucket with stacked-tensor arguments, except the batched call); graph "
+                         "rows replay the same launches from a CUDA graph"}
     del graphs
     print(json.dumps(line), flush=True)
     return 0 if same else 1

@@ -126,6 +126,42 @@ def _stream(stream) -> int:
     return int(stream)
 
 
+def _rows_contiguous(x: torch.Tensor) -> bool:
+    """Is every x[i] laid out contiguously (row-major over the dimensions after
+    the first)?"""
+    expect = 1
+    for size, st in zip(reversed(x.shape[1:]), reversed(x.stride()[1:])):
+        if size != 1 and st != expect:
+            return False
+        expect *= size
+    return True
+
+
+def _rows(x, count: int, dtype, n: int, what: str, check: bool = True):
+    """Host array of `count` device pointers, one per rank buffer.  `x` is a
+    sequence of tensors (one per buffer) or one CUDA tensor whose first
+    dimension indexes the buffers, each of which is contiguous (for example a
+    [K, N] tensor); the stacked form is checked once, whatever `count` is."""
+    if not isinstance(x, torch.Tensor):
+        if check:
+            _need(x, count, dtype, n, what)
+        return _ptrs(x)
+    if check:
+        if not x.is_cuda or x.dtype != dtype:
+            raise ValueError(f"{what}: need a CUDA {dtype} tensor")
+        dev = torch.cuda.current_device()
+        if x.device.index != dev:
+            raise ValueError(f"{what}: tensor on cuda:{x.device.index}, current device is cuda:{dev}")
+        if x.dim() < 2 or x.shape[0] != count:
+            raise ValueError(f"{what}: expected a tensor of {count} rows, got shape {tuple(x.shape)}")
+        if not _rows_contiguous(x):
+            raise ValueError(f"{what}: every row must be contiguous")
+        if x.numel() // max(count, 1) < n:
+            raise ValueError(f"{what}: rows of {x.numel() // max(count, 1)} elements, need {n}")
+    base, step = x.data_ptr(), x.stride(0) * x.element_size()
+    return (ctypes.c_void_p * count)(*[base + i * step for i in range(count)])
+
+
 def _need(ts: Sequence[torch.Tensor], count: int, dtype, n: int, what: str):
     if len(ts) != count:
         raise ValueError(f"{what}: expected {count} tensors, got {len(ts)}")
@@ -142,40 +178,54 @@ def _need(ts: Sequence[torch.Tensor], count: int, dtype, n: int, what: str):
             raise ValueError(f"{what}: tensor of {t.numel()} elements, need {n}")
 
 
-def dpr_reduce_scatter(inputs: Sequence[torch.Tensor], K: int, M: int, N: int,
-                       outputs: Sequence[torch.Tensor], mode=RING_FP32, scale: float | None = None,
-                       accumulate: bool = False, stream=None) -> None:
-    """inputs[m*K + r]: bf16 (N,), rank r micro-batch m; outputs[j]: fp32 (N/K,)."""
-    if N > 0:
-        _need(inputs, M * K, torch.bfloat16, N, "inputs")
-        _need(outputs, K, torch.float32, N // K if K else 0, "outputs")
-    st = lib().dpr_reduce_scatter(_ptrs(inputs), K, M, N, _ptrs(outputs), _MODES[mode],
+def dpr_reduce_scatter(inputs, K: int, M: int, N: int, outputs, mode=RING_FP32,
+                       scale: float | None = None, accumulate: bool = False,
+                       stream=None) -> None:
+    """inputs[m*K + r]: bf16 (N,), rank r micro-batch m; outputs[j]: fp32 (N/K,).
+    Either argument may also be one tensor of M*K (K) contiguous rows."""
+    chk = N > 0
+    ins = _rows(inputs, M * K, torch.bfloat16, N, "inputs", chk)
+    outs = _rows(outputs, K, torch.float32, N // K if K else 0, "outputs", chk)
+    st = lib().dpr_reduce_scatter(ins, K, M, N, outs, _MODES[mode],
                                   1.0 / K if scale is None else scale, int(bool(accumulate)),
                                   _stream(stream))
     _check("dpr_reduce_scatter", st)
 
 
-def dpr_reduce_scatter_batch(inputs: Sequence[Sequence[torch.Tensor]], K: int, M: int,
-                             N: Sequence[int], outputs: Sequence[Sequence[torch.Tensor]],
+def _member_rows(x, n: int, count: int, dtype, sizes: Sequence[int], what: str):
+    """Pointers of n members' `count` buffers, member after member.  `x` is a
+    sequence with one entry per member (each a sequence of tensors or one
+    tensor of `count` rows), or one tensor [n, count, ...] whose rows are
+    contiguous, checked once."""
+    if isinstance(x, torch.Tensor):
+        if x.dim() < 3 or x.shape[0] != n or x.shape[1] != count:
+            raise ValueError(f"{what}: expected a tensor of {n} members of {count} rows, "
+                             f"got shape {tuple(x.shape)}")
+        if x.stride(0) != count * x.stride(1):
+            raise ValueError(f"{what}: members must be laid out back to back")
+        # merging the first two dimensions is a view, never a copy, given the strides
+        return _rows(x.flatten(0, 1), n * count, dtype, max(sizes, default=0), what)
+    if len(x) != n:
+        raise ValueError(f"{what}: need one entry per member")
+    arrs = [_rows(x[i], count, dtype, sizes[i], f"{what}[{i}]", sizes[i] > 0) for i in range(n)]
+    for i, a in enumerate(arrs):
+        if len(a) != count:
+            raise ValueError(f"{what}[{i}]: expected {count} buffers, got {len(a)}")
+    return (ctypes.c_void_p * (n * count))(*[p for a in arrs for p in a])
+
+
+def dpr_reduce_scatter_batch(inputs, K: int, M: int, N: Sequence[int], outputs,
                              mode=RING_FP32, scale: float | None = None, accumulate: bool = False,
                              stream=None) -> None:
-    """Member i: inputs[i][m*K + r] bf16 (N[i],), outputs[i][j] fp32 (N[i]/K,).
-    The members must be independent (no output overlapping another member's
-    outputs or any input)."""
+    """Member i: inputs[i][m*K + r] bf16 (N[i],), outputs[i][j] fp32 (N[i]/K,);
+    inputs may also be one tensor [n, M*K, >= max N], outputs one tensor
+    [n, K, >= max N/K].  The members must be independent (no output
+    overlapping another member's outputs or any input)."""
     n = len(N)
-    if len(inputs) != n or len(outputs) != n:
-        raise ValueError("inputs, N and outputs need one entry per member")
-    flat_in, flat_out = [], []
-    for i in range(n):
-        if N[i] > 0:
-            _need(inputs[i], M * K, torch.bfloat16, N[i], f"inputs[{i}]")
-            _need(outputs[i], K, torch.float32, N[i] // K if K else 0, f"outputs[{i}]")
-        if len(inputs[i]) != M * K or len(outputs[i]) != K:
-            raise ValueError(f"member {i}: expected {M * K} inputs and {K} outputs")
-        flat_in += list(inputs[i])
-        flat_out += list(outputs[i])
+    ins = _member_rows(inputs, n, M * K, torch.bfloat16, list(N), "inputs")
+    outs = _member_rows(outputs, n, K, torch.float32, [x // K if K else 0 for x in N], "outputs")
     n_arr = (ctypes.c_int64 * max(n, 1))(*N)
-    st = lib().dpr_reduce_scatter_batch(n, _ptrs(flat_in), K, M, n_arr, _ptrs(flat_out),
+    st = lib().dpr_reduce_scatter_batch(n, ins, K, M, n_arr, outs,
                                         _MODES[mode], 1.0 / K if scale is None else scale,
                                         int(bool(accumulate)), _stream(stream))
     _check("dpr_reduce_scatter_batch", st)
@@ -194,11 +244,12 @@ def dpr_reduce_scatter_bf16(inputs: Sequence[torch.Tensor], K: int, M: int, N: i
                             outputs: Sequence[torch.Tensor], mode=RING_FP32,
                             scale: float | None = None, accumulate: bool = False,
                             stream=None) -> None:
-    """inputs[m*K + r]: bf16 (N,); outputs[j]: bf16 partition shard (N/K,)."""
-    if N > 0:
-        _need(inputs, M * K, torch.bfloat16, N, "inputs")
-        _need(outputs, K, torch.bfloat16, N // K if K else 0, "outputs")
-    st = lib().dpr_reduce_scatter_bf16(_ptrs(inputs), K, M, N, _ptrs(outputs), _MODES[mode],
+    """inputs[m*K + r]: bf16 (N,); outputs[j]: bf16 partition shard (N/K,).
+    Either argument may also be one tensor of contiguous rows."""
+    chk = N > 0
+    ins = _rows(inputs, M * K, torch.bfloat16, N, "inputs", chk)
+    outs = _rows(outputs, K, torch.bfloat16, N // K if K else 0, "outputs", chk)
+    st = lib().dpr_reduce_scatter_bf16(ins, K, M, N, outs, _MODES[mode],
                                        1.0 / K if scale is None else scale, int(bool(accumulate)),
                                        _stream(stream))
     _check("dpr_reduce_scatter_bf16", st)
@@ -215,22 +266,23 @@ def dpr_cast_bf16_to_fp32(inp: torch.Tensor, out: torch.Tensor, stream=None) -> 
 
 def dpr_allgather(shards: Sequence[torch.Tensor], K: int, N: int,
                   outputs: Sequence[torch.Tensor], stream=None) -> None:
-    """shards[j]: bf16 (N/K,); outputs[r]: bf16 (N,)."""
-    if N > 0:
-        _need(shards, K, torch.bfloat16, N // K if K else 0, "shards")
-        _need(outputs, K, torch.bfloat16, N, "outputs")
-    _check("dpr_allgather", lib().dpr_allgather(_ptrs(shards), K, N, _ptrs(outputs),
-                                                _stream(stream)))
+    """shards[j]: bf16 (N/K,); outputs[r]: bf16 (N,).  Either argument may also
+    be one tensor of K contiguous rows."""
+    chk = N > 0
+    sh = _rows(shards, K, torch.bfloat16, N // K if K else 0, "shards", chk)
+    outs = _rows(outputs, K, torch.bfloat16, N, "outputs", chk)
+    _check("dpr_allgather", lib().dpr_allgather(sh, K, N, outs, _stream(stream)))
 
 
 def dpr_allreduce(inputs: Sequence[torch.Tensor], K: int, N: int,
                   outputs: Sequence[torch.Tensor], mode=RING_FP32, scale: float | None = None,
                   stream=None) -> None:
-    """inputs[r], outputs[r]: bf16 (N,); outputs may be the inputs (in place)."""
-    if N > 0:
-        _need(inputs, K, torch.bfloat16, N, "inputs")
-        _need(outputs, K, torch.bfloat16, N, "outputs")
-    st = lib().dpr_allreduce(_ptrs(inputs), K, N, _ptrs(outputs), _MODES[mode],
+    """inputs[r], outputs[r]: bf16 (N,); outputs may be the inputs (in place).
+    Either argument may also be one tensor of K contiguous rows."""
+    chk = N > 0
+    ins = _rows(inputs, K, torch.bfloat16, N, "inputs", chk)
+    outs = _rows(outputs, K, torch.bfloat16, N, "outputs", chk)
+    st = lib().dpr_allreduce(ins, K, N, outs, _MODES[mode],
                              1.0 / K if scale is None else scale, _stream(stream))
     _check("dpr_allreduce", st)
 
@@ -288,8 +340,8 @@ def dpr_flatten_plan_create(srcs: Sequence[Sequence[torch.Tensor]], numel: Seque
 
 def dpr_flatten_bucket(plan: FlattenPlan, dst: Sequence[torch.Tensor], stream=None) -> None:
     """dst[r]: rank r's flat bucket, bf16 (bucket_numel,)."""
-    _need(dst, plan.K, torch.bfloat16, plan.bucket_numel, "dst")
-    _check("dpr_flatten_bucket", lib().dpr_flatten_bucket(plan.handle, _ptrs(dst), _stream(stream)))
+    d = _rows(dst, plan.K, torch.bfloat16, plan.bucket_numel, "dst")
+    _check("dpr_flatten_bucket", lib().dpr_flatten_bucket(plan.handle, d, _stream(stream)))
 
 
 def dpr_flatten_plan_destroy(plan: FlattenPlan) -> None:
@@ -340,8 +392,8 @@ def dpr_reduce_scatter_fragments(plan: FragmentsPlan, outputs: Sequence[torch.Te
                                  mode=RING_FP32, scale: float | None = None,
                                  accumulate: bool = False, stream=None) -> None:
     """outputs[j]: fp32 shard j of the bucket (bucket_numel / K,)."""
-    _need(outputs, plan.K, torch.float32, plan.bucket_numel // plan.K, "outputs")
-    st = lib().dpr_reduce_scatter_fragments(plan.handle, _ptrs(outputs), _MODES[mode],
+    outs = _rows(outputs, plan.K, torch.float32, plan.bucket_numel // plan.K, "outputs")
+    st = lib().dpr_reduce_scatter_fragments(plan.handle, outs, _MODES[mode],
                                             1.0 / plan.K if scale is None else scale,
                                             int(bool(accumulate)), _stream(stream))
     _check("dpr_reduce_scatter_fragments", st)
@@ -428,8 +480,8 @@ def dpr_reduce_scatter_coalesced(plan: CoalescedPlan, outputs: Sequence[torch.Te
                                  mode=RING_FP32, scale: float | None = None,
                                  accumulate: bool = False, stream=None) -> None:
     """outputs[j]: rank j's fp32 partition (plan.partition_numel,)."""
-    _need(outputs, plan.K, torch.float32, plan.partition_numel, "outputs")
-    st = lib().dpr_reduce_scatter_coalesced(plan.handle, _ptrs(outputs), _MODES[mode],
+    outs = _rows(outputs, plan.K, torch.float32, plan.partition_numel, "outputs")
+    st = lib().dpr_reduce_scatter_coalesced(plan.handle, outs, _MODES[mode],
                                             1.0 / plan.K if scale is None else scale,
                                             int(bool(accumulate)), _stream(stream))
     _check("dpr_reduce_scatter_coalesced", st)
@@ -439,8 +491,8 @@ def dpr_allgather_coalesced(plan: CoalescedPlan, shards: Sequence[torch.Tensor],
                             stream=None) -> None:
     """shards[j]: rank j's bf16 partition (plan.partition_numel,); writes the
     plan's bound parameter tensors."""
-    _need(shards, plan.K, torch.bfloat16, plan.partition_numel, "shards")
-    _check("dpr_allgather_coalesced", lib().dpr_allgather_coalesced(plan.handle, _ptrs(shards),
+    sh = _rows(shards, plan.K, torch.bfloat16, plan.partition_numel, "shards")
+    _check("dpr_allgather_coalesced", lib().dpr_allgather_coalesced(plan.handle, sh,
                                                                     _stream(stream)))
 
 

@@ -299,3 +299,47 @@ def test_fragments_batch_over_several_launches(K, n_buckets):
             H.assert_f32_equal(outs[b][j].cpu().numpy(), want[j], f"bucket {b} shard {j}")
     for pl in plans:
         pl.close()
+
+
+def test_stacked_tensor_arguments_equal_lists():
+    """The binding takes one tensor of contiguous rows in place of a list of
+    rank buffers (checked once, not buffer by buffer): same pointers, same
+    bits; rows that are not contiguous are refused on the host."""
+    dev = H.device()
+    K, M, N = 8, 2, 8 * 16 * 4096
+    S = N // K
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    x = torch.empty(M * K, N, dtype=torch.bfloat16, device=dev).normal_(0, 1e-3, generator=g)
+    a = torch.empty(K, S, device=dev)
+    b = torch.empty(K, S, device=dev)
+    dpr.dpr_reduce_scatter(x, K, M, N, a, mode=ring.HOP_BF16)
+    dpr.dpr_reduce_scatter(list(x.unbind(0)), K, M, N, list(b.unbind(0)), mode=ring.HOP_BF16)
+    full_a = torch.empty(K, N, dtype=torch.bfloat16, device=dev)
+    full_b = torch.empty(K, N, dtype=torch.bfloat16, device=dev)
+    shards = x[:K, :S]                    # rows of S elements, N apart
+    dpr.dpr_allgather(shards, K, N, full_a)
+    dpr.dpr_allgather([shards[j] for j in range(K)], K, N, list(full_b.unbind(0)))
+    ar_a = torch.empty(K, N, dtype=torch.bfloat16, device=dev)
+    dpr.dpr_allreduce(x[K:], K, N, ar_a)
+    ar_b = [torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+    dpr.dpr_allreduce(list(x[K:].unbind(0)), K, N, ar_b)
+    # a batch of 3 members as one [3, M*K, N] tensor and one [3, K, S] tensor
+    xb = x.unsqueeze(0).repeat(3, 1, 1)
+    ob = torch.empty(3, K, S, device=dev)
+    dpr.dpr_reduce_scatter_batch(xb, K, M, [N] * 3, ob, mode=ring.HOP_BF16)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.equal(full_a.view(torch.int16), full_b.view(torch.int16))
+    for r in range(K):
+        assert torch.equal(ar_a[r].view(torch.int16), ar_b[r].view(torch.int16))
+    for i in range(3):
+        assert torch.equal(ob[i].view(torch.int32), a.view(torch.int32))
+    with pytest.raises(ValueError):
+        dpr.dpr_reduce_scatter(x.t(), K, M, N, a)                        # rows not contiguous
+    with pytest.raises(ValueError):
+        dpr.dpr_reduce_scatter(x[: M * K - 1], K, M, N, a)               # too few rows
+    with pytest.raises(ValueError):
+        dpr.dpr_reduce_scatter(x, K, M, N, a[:, : S - 1])                # rows too short
+    with pytest.raises(ValueError):
+        dpr.dpr_reduce_scatter_batch(xb.transpose(0, 1), K, M, [N] * 3, ob)
