@@ -882,7 +882,7 @@ def run_sequence_bench(args):
     buckets of 4 MiB per rank at K=8 (2 micro-batches, ring fp32, x1/8),
     reduce-scattered with plain launches, with programmatic dependent launches
     (one call per bucket), and in one batched call; then the same 64 buckets
-    all-gathered with plain and with programmatic launches.  Each figure is
+    all-gathered with plain and programmatic launches and in one batched call.  Each figure is
     the sequence's algorithmic bytes over its CUDA-event time, averaged over
     --steps sequences (4.8 GB per reduce-scatter sequence, far larger than
     L2, so no flush is needed).  The three reduce-scatter forms must give the
@@ -934,6 +934,9 @@ def run_sequence_bench(args):
     def ag_single():
         for b in range(nb):
             dpr.dpr_allgather(shards[b], K, N, full_l[b], stream=s)
+
+    def ag_batch():
+        dpr.dpr_allgather_batch(shards, K, [N] * nb, full, stream=s)
 
     def timed(fn):
         for _ in range(args.warmup):
@@ -989,6 +992,10 @@ def run_sequence_bench(args):
     r, g = graphed(ag_single)
     graphs.append(g)
     t_ag_pdl_g = timed(r)
+    t_ag_batch = timed(ag_batch)
+    r, g = graphed(ag_batch)
+    graphs.append(g)
+    t_ag_batch_g = timed(r)
     dpr.dpr_set_programmatic_launch(prev)
     same = all(torch.equal(outs["plain"].view(torch.int32), outs[k].view(torch.int32))
                for k in ("pdl", "batch"))
@@ -1024,8 +1031,10 @@ def run_sequence_bench(args):
                                "bytes": rs_bytes, "bit_identical": same},
             "allgather": {"plain_launches": fig(ag_bytes, t_ag_plain),
                           "programmatic_launches": fig(ag_bytes, t_ag_pdl),
+                          "one_batched_call": fig(ag_bytes, t_ag_batch),
                           "graph_plain_launches": fig(ag_bytes, t_ag_plain_g),
                           "graph_programmatic_launches": fig(ag_bytes, t_ag_pdl_g),
+                          "graph_one_batched_call": fig(ag_bytes, t_ag_batch_g),
                           "bytes": ag_bytes},
             "host_cost": host,
             "host_note": "eager rows include the Python binding's per-call cost (one call per "

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     FlattenPlan,
     FragmentsPlan,
     dpr_allgather,
+    dpr_allgather_batch,
     dpr_allreduce,
     dpr_allgather_coalesced,
     dpr_bucket_assign,

@@ -30,6 +30,7 @@ _SIGS = {
     "dpr_reduce_scatter_batch": [ctypes.c_int, _pp, ctypes.c_int, ctypes.c_int, _i64p, _pp,
                                  ctypes.c_int, ctypes.c_float, ctypes.c_int, _c_p],
     "dpr_allgather": [_pp, ctypes.c_int, ctypes.c_int64, _pp, _c_p],
+    "dpr_allgather_batch": [ctypes.c_int, _pp, ctypes.c_int, _i64p, _pp, _c_p],
     "dpr_reduce_scatter_bf16": [_pp, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _pp, ctypes.c_int,
                                 ctypes.c_float, ctypes.c_int, _c_p],
     "dpr_cast_bf16_to_fp32": [_c_p, _c_p, ctypes.c_int64, _c_p],
@@ -272,6 +273,18 @@ def dpr_allgather(shards: Sequence[torch.Tensor], K: int, N: int,
     sh = _rows(shards, K, torch.bfloat16, N // K if K else 0, "shards", chk)
     outs = _rows(outputs, K, torch.bfloat16, N, "outputs", chk)
     _check("dpr_allgather", lib().dpr_allgather(sh, K, N, outs, _stream(stream)))
+
+
+def dpr_allgather_batch(shards, K: int, N: Sequence[int], outputs, stream=None) -> None:
+    """Member i: shards[i][j] bf16 (N[i]/K,), outputs[i][r] bf16 (N[i],);
+    shards may also be one tensor [n, K, >= max N/K], outputs one tensor
+    [n, K, >= max N].  The members must be independent (no output overlapping
+    another member's outputs or shards)."""
+    n = len(N)
+    sh = _member_rows(shards, n, K, torch.bfloat16, [x // K if K else 0 for x in N], "shards")
+    outs = _member_rows(outputs, n, K, torch.bfloat16, list(N), "outputs")
+    n_arr = (ctypes.c_int64 * max(n, 1))(*N)
+    _check("dpr_allgather_batch", lib().dpr_allgather_batch(n, sh, K, n_arr, outs, _stream(stream)))
 
 
 def dpr_allreduce(inputs: Sequence[torch.Tensor], K: int, N: int,

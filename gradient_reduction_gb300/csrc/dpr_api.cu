@@ -276,8 +276,14 @@ dpr_status dpr_cast_bf16_to_fp32(const void* in, float* out, int64_t n, void* st
                                    static_cast<cudaStream_t>(stream)));
 }
 
-dpr_status dpr_allgather(const void* const* shard, int K, int64_t N, void* const* out,
-                         void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The checks of dpr_allgather, filling the parameter block and the access
+// width on success (nothing is launched).
+dpr_status prepare_allgather(const void* const* shard, int K, int64_t N, void* const* out,
+                             AgParams* p, int* width) {
     dpr_status st = check_kn(K, N);
     if (st != DPR_OK) return st;
     if (N == 0) return DPR_OK;
@@ -304,18 +310,73 @@ dpr_status dpr_allgather(const void* const* shard, int K, int64_t N, void* const
             if (overlaps(a, outs[r])) return DPR_ERR_ALIAS;
         }
     }
-    AgParams p;
-    std::memset(&p, 0, sizeof(p));
+    std::memset(p, 0, sizeof(*p));
     for (int r = 0; r < K; ++r) {
-        p.shard[r] = static_cast<const uint16_t*>(shard[r]);
-        p.out[r] = static_cast<uint16_t*>(out[r]);
+        p->shard[r] = static_cast<const uint16_t*>(shard[r]);
+        p->out[r] = static_cast<uint16_t*>(out[r]);
     }
-    p.S = S;
-    p.tiles_per_chunk = uint64_t((S + kAgTile - 1) / kAgTile);
-    p.in_place = in_place_mask;
-    p.K = K;
-    const int width = access_width(S, a32, a16);
+    p->S = S;
+    p->tiles_per_chunk = uint64_t((S + kAgTile - 1) / kAgTile);
+    p->in_place = in_place_mask;
+    p->K = K;
+    p->order = kAfterPrevious;
+    *width = access_width(S, a32, a16);
+    return DPR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dpr_status dpr_allgather(const void* const* shard, int K, int64_t N, void* const* out,
+                         void* stream) {
+    AgParams p;
+    int width = 0;
+    dpr_status st = prepare_allgather(shard, K, N, out, &p, &width);
+    if (st != DPR_OK || N == 0) return st;
     return cuda_status(launch_allgather(p, width, static_cast<cudaStream_t>(stream)));
+}
+
+dpr_status dpr_allgather_batch(int n, const void* const* shard, int K, const int64_t* N,
+                               void* const* out, void* stream) {
+    if (n < 0) return DPR_ERR_INVALID_ARG;
+    if (n > DPR_MAX_BATCH) return DPR_ERR_UNSUPPORTED;
+    if (n == 0) return DPR_OK;
+    if (!shard || !N || !out) return DPR_ERR_INVALID_ARG;
+    if (K < 2 || K > DPR_MAX_RANKS) return DPR_ERR_INVALID_ARG;
+    std::vector<AgParams> prm(static_cast<size_t>(n));
+    std::vector<int> width(static_cast<size_t>(n), 0);
+    std::vector<OwnedSpan> outs;
+    std::vector<OwnedSpan> shards;
+    for (int i = 0; i < n; ++i) {
+        const void* const* sh_i = shard + size_t(i) * K;
+        void* const* out_i = out + size_t(i) * K;
+        dpr_status st = prepare_allgather(sh_i, K, N[i], out_i, &prm[i], &width[i]);
+        if (st != DPR_OK) return st;
+        if (N[i] == 0) continue;
+        for (int r = 0; r < K; ++r) {
+            outs.push_back({span_of(out_i[r], uint64_t(N[i]) * 2), i});
+            shards.push_back({span_of(sh_i[r], uint64_t(N[i] / K) * 2), i});
+        }
+    }
+    // members are independent: no output touches another member's output or
+    // shard (a member's own in-place shard is checked above)
+    std::sort(outs.begin(), outs.end(),
+              [](const OwnedSpan& a, const OwnedSpan& b) { return a.s.lo < b.s.lo; });
+    for (size_t q = 1; q < outs.size(); ++q)
+        if (outs[q].s.lo < outs[q - 1].s.hi) return DPR_ERR_ALIAS;
+    for (const OwnedSpan& x : shards)
+        if (overlaps_other(outs, x.s, x.owner)) return DPR_ERR_ALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool first = true;
+    for (int i = 0; i < n; ++i) {
+        if (N[i] == 0) continue;
+        prm[i].order = first ? kAfterPrevious : kBesidePrevious;
+        first = false;
+        const cudaError_t e = launch_allgather(prm[i], width[i], s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return DPR_OK;
 }
 
 dpr_status dpr_allreduce(const void* const* in, int K, int64_t N, void* const* out, int mode,

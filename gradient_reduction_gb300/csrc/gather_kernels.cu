@@ -19,10 +19,9 @@ namespace {
 // K-1 blocks from L2.  Every block then writes a single contiguous stream.
 // In the in-place form (shard j inside replica j) the block for r == j has
 // nothing to do, so no block writes memory that another block reads.
+// Copies the tile of block b (one tile of shard j into replica r).
 template <int W>
-__global__ void __launch_bounds__(kThreads) ag_vec(const __grid_constant__ AgParams p) {
-    order_enter(p.order);
-    const uint64_t b = blockIdx.x;
+__device__ __forceinline__ void ag_tile(const AgParams& p, uint64_t b) {
     const int r = int(b % uint64_t(p.K));
     const uint64_t g = b / uint64_t(p.K);
     const uint64_t j = g / p.tiles_per_chunk;
@@ -54,10 +53,19 @@ __global__ void __launch_bounds__(kThreads) ag_vec(const __grid_constant__ AgPar
     }
 }
 
+template <int W>
+__global__ void __launch_bounds__(kThreads) ag_vec(const __grid_constant__ AgParams p) {
+    order_start(p.order);
+    order_enter(p.order);
+    ag_tile<W>(p, blockIdx.x);
+    order_exit(p.order);
+}
+
 __global__ void __launch_bounds__(kThreads) ag_scalar(const __grid_constant__ AgParams p) {
     const int j = blockIdx.y, K = p.K;
     const uint64_t S = uint64_t(p.S), base = uint64_t(j) * S;
     const uint16_t* const src = p.shard[j];
+    order_start(p.order);
     order_enter(p.order);
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < S;
          t += uint64_t(gridDim.x) * kThreads) {
@@ -65,6 +73,7 @@ __global__ void __launch_bounds__(kThreads) ag_scalar(const __grid_constant__ Ag
         for (int r = 0; r < K; ++r)
             if (!(((p.in_place >> j) & 1u) && r == j)) p.out[r][base + t] = v;
     }
+    order_exit(p.order);
 }
 
 // ---- flat-bucket gather ----------------------------------------------------------

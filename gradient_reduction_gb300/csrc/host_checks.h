@@ -42,6 +42,22 @@ inline bool any_overlap(std::vector<Span> a, const std::vector<Span>& b) {
     return false;
 }
 
+// A span with the index of the batch member it belongs to.
+struct OwnedSpan {
+    Span s;
+    int owner;
+};
+
+// Does `x` (of member `owner`) overlap a span of `sorted` that belongs to
+// another member?  `sorted` must be pairwise disjoint and sorted by start.
+inline bool overlaps_other(const std::vector<OwnedSpan>& sorted, const Span& x, int owner) {
+    auto it = std::upper_bound(sorted.begin(), sorted.end(), x.lo,
+                               [](uintptr_t v, const OwnedSpan& y) { return v < y.s.hi; });
+    for (; it != sorted.end() && it->s.lo < x.hi; ++it)
+        if (it->owner != owner && overlaps(it->s, x)) return true;
+    return false;
+}
+
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // cudaMalloc a device copy of `src` and enqueue the copy on `st`.

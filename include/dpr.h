@@ -153,6 +153,21 @@ dpr_status dpr_allgather(const void* const* shard, int K, int64_t N, void* const
                          void* stream);
 
 /*
+ * n all-gathers in one call: the parameter all-gathers of ZeRO-3 that a
+ * forward pass issues one layer after another (DeepSpeed ZeRO-3 source
+ * walkthrough, sections 1 and 2.1).  The result is that of n dpr_allgather
+ * calls in order; member i uses shard[i*K .. (i+1)*K), N[i] and
+ * out[i*K .. (i+1)*K) (host arrays), and is checked as dpr_allgather checks
+ * it (its own in-place form included).  In addition no output of any member
+ * may overlap another member's outputs or shards (DPR_ERR_ALIAS), so the
+ * members are independent and run beside one another as described for
+ * dpr_reduce_scatter_batch.  One kernel per member with N[i] > 0.
+ * n: 0..DPR_MAX_BATCH.
+ */
+dpr_status dpr_allgather_batch(int n, const void* const* shard, int K, const int64_t* N,
+                               void* const* out, void* stream);
+
+/*
  * Ring all-reduce = reduce-scatter + all-gather (lecture section 2.2), fused
  * into one pass: each element's ring-order sum (as in dpr_reduce_scatter,
  * M = 1) is multiplied by scale, rounded once to bf16, and written to every

@@ -35,7 +35,7 @@ def _declared():
 
 def test_exports_every_declared_function(L):
     names = _declared()
-    assert len(names) == 34
+    assert len(names) == 35
     for n in names:
         assert hasattr(L, n), n
 
@@ -332,3 +332,23 @@ print(st, L.dpr_last_cuda_error())
         assert err != 0
     else:
         assert err == 0
+
+
+def test_allgather_batch_rejections(L):
+    K, N = 4, 64
+    S = N // K
+    ag = L.dpr_allgather_batch
+    sh = _bufs(2 * K, 1 << 20)
+    outs = _bufs(2 * K, 1 << 20, BASE + (1 << 30))
+    n2 = (ctypes.c_int64 * 2)(N, N)
+    assert ag(0, None, K, None, None, None) == OK
+    assert ag(-1, _arr(sh), K, n2, _arr(outs), None) == INVALID
+    assert ag(4097, _arr(sh), K, n2, _arr(outs), None) == UNSUP
+    assert ag(2, _arr(sh), 1, n2, _arr(outs), None) == INVALID                 # K < 2
+    assert ag(2, _arr(sh), K, (ctypes.c_int64 * 2)(N, N + 1), _arr(outs), None) == INVALID
+    # member 1 writes into member 0's output
+    assert ag(2, _arr(sh), K, n2, _arr(outs[:K] + [outs[1] + 64] + outs[K + 1:]), None) == ALIAS
+    # member 1 writes over member 0's shard
+    assert ag(2, _arr(sh), K, n2, _arr(outs[:K] + [sh[0]] + outs[K + 1:]), None) == ALIAS
+    # member 0 writes over member 1's shard
+    assert ag(2, _arr(sh), K, n2, _arr([sh[K + 2] - 2 * S] + outs[1:]), None) == ALIAS

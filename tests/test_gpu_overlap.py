@@ -343,3 +343,81 @@ def test_stacked_tensor_arguments_equal_lists():
         dpr.dpr_reduce_scatter(x, K, M, N, a[:, : S - 1])                # rows too short
     with pytest.raises(ValueError):
         dpr.dpr_reduce_scatter_batch(xb.transpose(0, 1), K, M, [N] * 3, ob)
+
+
+AG_BATCHES = [  # (K, member sizes, in-place members)
+    (8, [8 * 16 * 600, 0, 8 * 8 * 33, 8 * 13, 8 * 8192 * 3 + 8 * 16], {0, 4}),
+    (4, [4 * 16 * 4096] * 5 + [4 * 5], {2}),
+    (5, [5 * 16 * 301, 5 * 9, 5 * 8192 * 2], set()),
+]
+
+
+@pytest.mark.parametrize("K,sizes,in_place", AG_BATCHES)
+def test_allgather_batch_after_the_reduce_scatter_that_wrote_its_shards(K, sizes, in_place):
+    """bf16 partition shards written by reduce-scatters on the same stream, then
+    all-gathered in one batched call (members in place or not): the result
+    equals single calls and the oracle's reduce-scatter followed by its
+    all-gather."""
+    dev = H.device()
+    s = torch.cuda.Stream()
+    host_x, outs, shards, ref = [], [], [], []
+    for i, N in enumerate(sizes):
+        S = N // K
+        hx = [_host_bits(N, syn.stream_key(80 + i, r)) for r in range(K)]
+        host_x.append(hx)
+        xi = [_dev(a, dev) for a in hx]
+        o = [torch.full((N,), 1.0, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+        if i in in_place:
+            sh = [o[j][j * S:(j + 1) * S] for j in range(K)]
+        else:
+            sh = [torch.empty(S, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+        if N > 0:
+            dpr.dpr_reduce_scatter_bf16(xi, K, 1, N, sh, stream=s)
+        outs.append(o)
+        shards.append(sh)
+        ref.append([torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(K)])
+    dpr.dpr_allgather_batch(shards, K, sizes, outs, stream=s)
+    for i, N in enumerate(sizes):
+        dpr.dpr_allgather(shards[i], K, N, ref[i], stream=s)
+    s.synchronize()
+    for i, N in enumerate(sizes):
+        if N == 0:
+            continue
+        want_sh, _ = ring.reduce_scatter_bf16(host_x[i], K, 1, ring.RING_FP32, 1.0 / K)
+        want, _ = ring.allgather(want_sh, K)
+        for r in range(K):
+            assert torch.equal(outs[i][r].view(torch.int16), ref[i][r].view(torch.int16)), \
+                f"member {i} replica {r}: batch differs from single calls"
+            H.assert_bf16_equal(H.bits(outs[i][r]), want[r], f"member {i} replica {r}")
+
+
+def test_deep_batches_complete_in_order():
+    """4096 one-block members in each batched call (the deepest chain of grids
+    the calls accept), followed on the stream by work that reads every
+    member's output: every member has completed before it."""
+    dev = H.device()
+    K, n = 4, 4096
+    N = K * 16
+    x = torch.empty(n, K, N, dtype=torch.bfloat16, device=dev).normal_(0, 1.0)
+    out = torch.zeros(n, K, N // K, device=dev)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    dpr.dpr_reduce_scatter_batch(x, K, 1, [N] * n, out, stream=s)
+    with torch.cuda.stream(s):
+        total = out.sum(dim=(1, 2))             # reads every member's output after the batch
+    full = torch.zeros(n, K, N, dtype=torch.bfloat16, device=dev)
+    shards = torch.as_strided(x, (n, K, N // K), (K * N, N, 1))    # rank j's first chunk
+    dpr.dpr_allgather_batch(shards, K, [N] * n, full, stream=s)
+    with torch.cuda.stream(s):
+        copied = full.float().sum(dim=(1, 2))
+    s.synchronize()
+    # what the stream read right after each batch is what the members finally wrote
+    assert torch.equal(total, out.sum(dim=(1, 2)))
+    assert torch.equal(copied, full.float().sum(dim=(1, 2)))
+    ref = torch.empty(K, N // K, device=dev)
+    for i in (0, 1, n // 2, n - 2, n - 1):
+        dpr.dpr_reduce_scatter(x[i], K, 1, N, ref)
+        torch.cuda.synchronize()
+        assert torch.equal(out[i].view(torch.int32), ref.view(torch.int32)), i
+    cat = shards.reshape(n, 1, N).expand(n, K, N)       # every replica: the K shards in order
+    assert torch.equal(full.view(torch.int16), cat.contiguous().view(torch.int16))
