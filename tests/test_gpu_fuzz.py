@@ -161,3 +161,53 @@ def test_fuzz_reduce_scatter_fragments(case):
     want, _ = ring.reduce_scatter(flat, K, 1, mode, scale, out_init=init if acc else None)
     for j in range(K):
         H.assert_f32_equal(outs[j].cpu().numpy(), want[j], f"K={K} P={P} shard {j}")
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_fuzz_batched_calls(case):
+    """Random batches of independent reduce-scatters and all-gathers: members of
+    random chunk lengths (empty ones included) and alignments, one K, M and mode
+    per batch, on a side stream (programmatic launches).  Every member equals
+    the oracle bit for bit."""
+    dev = H.device()
+    rng = random.Random(11000 + case)
+    nrng = np.random.default_rng(11000 + case)
+    K, M = rng.choice([2, 3, 4, 8, 16]), rng.choice([1, 2])
+    mode, acc = rng.choice(H.MODES), rng.random() < 0.5
+    n = rng.randint(1, 12)
+    Ss = [rng.choice([0] + SS) for _ in range(n)]
+    xs, xin, init, outs = [], [], [], []
+    for S in Ss:
+        N = K * S
+        x = [_spread_bf16(nrng, N, spread=rng.choice([4, 12])) for _ in range(M * K)]
+        off = rng.choice([0, 0, 1, 8])
+        xs.append(x)
+        xin.append([_dev_bf16(a, dev, off) for a in x])
+        i0 = [nrng.standard_normal(S).astype(np.float32) for _ in range(K)]
+        init.append(i0)
+        ooff = rng.choice([0, 0, 1, 4])
+        row = []
+        for a in i0:
+            b = torch.empty(S + 8, dtype=torch.float32, device=dev)
+            o = b[ooff:ooff + S]
+            o.copy_(torch.from_numpy(a))
+            row.append(o)
+        outs.append(row)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    dpr.dpr_reduce_scatter_batch(xin, K, M, [K * S for S in Ss], outs, mode=mode,
+                                 scale=1.0 / K, accumulate=acc, stream=s)
+    # all-gather the first micro-batch's chunk j of rank j, member by member
+    shards = [[xin[i][j][j * S:(j + 1) * S] for j in range(K)] for i, S in enumerate(Ss)]
+    full = [[torch.empty(K * S, dtype=torch.bfloat16, device=dev) for _ in range(K)] for S in Ss]
+    dpr.dpr_allgather_batch(shards, K, [K * S for S in Ss], full, stream=s)
+    s.synchronize()
+    for i, S in enumerate(Ss):
+        if S == 0:
+            continue
+        want, _ = ring.reduce_scatter(xs[i], K, M, mode, 1.0 / K, out_init=init[i] if acc else None)
+        for j in range(K):
+            H.assert_f32_equal(outs[i][j].cpu().numpy(), want[j], f"member {i} shard {j}")
+        want_ag, _ = ring.allgather([xs[i][j][j * S:(j + 1) * S] for j in range(K)], K)
+        for r in range(K):
+            H.assert_bf16_equal(H.bits(full[i][r]), want_ag[r], f"member {i} replica {r}")

@@ -421,3 +421,49 @@ def test_deep_batches_complete_in_order():
         assert torch.equal(out[i].view(torch.int32), ref.view(torch.int32)), i
     cat = shards.reshape(n, 1, N).expand(n, K, N)       # every replica: the K shards in order
     assert torch.equal(full.view(torch.int16), cat.contiguous().view(torch.int16))
+
+
+def test_batched_calls_replay_from_a_cuda_graph():
+    """The batched calls captured in a CUDA graph (their programmatic launches
+    become programmatic edges) replay to the eager results, twice in a row."""
+    dev = H.device()
+    K, M, n, N = 8, 1, 6, 8 * 16 * 1024
+    S = N // K
+    g = torch.Generator(device=dev)
+    g.manual_seed(21)
+    x = torch.empty(n, M * K, N, dtype=torch.bfloat16, device=dev).normal_(0, 1e-3, generator=g)
+    eager_rs = torch.empty(n, K, S, device=dev)
+    eager_ag = torch.empty(n, K, N, dtype=torch.bfloat16, device=dev)
+    shards = torch.as_strided(x, (n, K, S), (M * K * N, N, 1))
+    dpr.dpr_reduce_scatter_batch(x, K, M, [N] * n, eager_rs)
+    dpr.dpr_allgather_batch(shards, K, [N] * n, eager_ag)
+    numel, buckets, grads = _fragment_buckets(dev, 4)
+    plans = [dpr.dpr_fragments_plan_create([[grads[r][p] for p in b.params] for r in range(4)],
+                                           [numel[p] for p in b.params], b.offsets, b.numel)
+             for b in buckets]
+    eager_fr = [torch.empty(4, b.numel // 4, device=dev) for b in buckets]
+    dpr.dpr_reduce_scatter_fragments_batch(plans, eager_fr)
+    torch.cuda.synchronize()
+    rs = torch.zeros_like(eager_rs)
+    ag = torch.zeros_like(eager_ag)
+    fr = [torch.zeros_like(t) for t in eager_fr]
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        dpr.dpr_reduce_scatter_batch(x, K, M, [N] * n, rs, stream=s)
+        dpr.dpr_allgather_batch(shards, K, [N] * n, ag, stream=s)
+        dpr.dpr_reduce_scatter_fragments_batch(plans, fr, stream=s)
+    for _ in range(2):
+        rs.zero_()
+        ag.zero_()
+        for t in fr:
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(rs.view(torch.int32), eager_rs.view(torch.int32))
+        assert torch.equal(ag.view(torch.int16), eager_ag.view(torch.int16))
+        for a, b in zip(fr, eager_fr):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    del graph
+    for pl in plans:
+        pl.close()
