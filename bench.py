@@ -922,6 +922,14 @@ def run_sequence_bench(args):
         dpr.dpr_reduce_scatter_batch(x, K, M, [N] * nb, outs["batch"], mode=dpr.RING_FP32,
                                      stream=s)
 
+    # persistent requests: every bucket's call checked once, started every step
+    reqs = [dpr.dpr_reduce_scatter_init(ins[b], K, M, N, out_l["pdl"][b], mode=dpr.RING_FP32)
+            for b in range(nb)]
+
+    def rs_requests():
+        for rq in reqs:
+            rq.start(s)
+
     def host_us(fn, calls):
         """Host time per call of fn (no synchronisation inside the loop)."""
         s.synchronize()
@@ -981,6 +989,7 @@ def run_sequence_bench(args):
         dpr.dpr_set_programmatic_launch(prev)
     dpr.dpr_set_programmatic_launch(True)
     t_rs_pdl = timed(lambda: rs_single("pdl"))
+    t_rs_req = timed(rs_requests)
     t_rs_batch = timed(rs_batch)
     t_ag_pdl = timed(ag_single)
     r, g = graphed(lambda: rs_single("pdl"))
@@ -1007,7 +1016,10 @@ def run_sequence_bench(args):
             for b in range(nb)], nb), 2),
         "stacked_args_us_per_call": round(host_us(lambda: rs_single("plain"), nb), 2),
         "batched_call_us_per_bucket": round(host_us(rs_batch, nb), 2),
+        "persistent_request_us_per_start": round(host_us(rs_requests, nb), 2),
     }
+    for rq in reqs:
+        rq.close()
     peak, kind = load_peaks()
 
     def fig(nbytes, t):
@@ -1024,6 +1036,7 @@ def run_sequence_bench(args):
             "peak": peak, "peak_kind": kind,
             "reduce_scatter": {"plain_launches": fig(rs_bytes, t_rs_plain),
                                "programmatic_launches": fig(rs_bytes, t_rs_pdl),
+                               "persistent_requests": fig(rs_bytes, t_rs_req),
                                "one_batched_call": fig(rs_bytes, t_rs_batch),
                                "graph_plain_launches": fig(rs_bytes, t_rs_plain_g),
                                "graph_programmatic_launches": fig(rs_bytes, t_rs_pdl_g),
@@ -1624,7 +1637,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage": "bf16 gradients and parameters, fp32 partitions",
-        "data": "synthetic (seeded counter-hash generator)",
+        "data": "synthetic (seeded counter-hash generator; Box-Muller normals, uniform parameters)",
         "config": common_config(1),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"K=8, the same five steps per step; {cores} processes, each "
@@ -1672,7 +1685,7 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(res["max_elapsed"] / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "storage": "bf16 gradients and parameters, fp32 partitions", "data": "synthetic (seeded counter-hash generator)",
+        "dtype": "f32", "storage": "bf16 gradients and parameters, fp32 partitions", "data": "synthetic (seeded counter-hash generator; Box-Muller normals, uniform parameters)",
         "config": common_config(world),
         "pct_of_peak": round(100 * value / world / peak, 2),
         "pct_of_peak_is": f"of the {peak_kind} HBM copy peak ({peak} GB/s); the step's "

@@ -15,11 +15,14 @@ from ._binding import (  # noqa: F401
     LIB_PATH,
     RING_FP32,
     DprError,
+    Request,
     FlattenPlan,
     FragmentsPlan,
     dpr_allgather,
     dpr_allgather_batch,
+    dpr_allgather_init,
     dpr_allreduce,
+    dpr_allreduce_init,
     dpr_allgather_coalesced,
     dpr_bucket_assign,
     dpr_cast_bf16_to_fp32,
@@ -42,6 +45,7 @@ from ._binding import (  # noqa: F401
     dpr_reduce_scatter_coalesced,
     dpr_reduce_scatter_fragments,
     dpr_reduce_scatter_fragments_batch,
+    dpr_reduce_scatter_init,
     dpr_set_programmatic_launch,
     dpr_strerror,
     dpr_version,

@@ -75,6 +75,13 @@ _SIGS = {
     "dpr_cost_dp_speedup": [ctypes.c_double, ctypes.c_int, ctypes.c_double, ctypes.c_double,
                             ctypes.c_double, ctypes.POINTER(ctypes.c_double)],
     "dpr_set_programmatic_launch": [ctypes.c_int, ctypes.POINTER(ctypes.c_int)],
+    "dpr_reduce_scatter_init": [ctypes.POINTER(_c_p), _pp, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int64, _pp, ctypes.c_int, ctypes.c_float, ctypes.c_int],
+    "dpr_allgather_init": [ctypes.POINTER(_c_p), _pp, ctypes.c_int, ctypes.c_int64, _pp],
+    "dpr_allreduce_init": [ctypes.POINTER(_c_p), _pp, ctypes.c_int, ctypes.c_int64, _pp,
+                           ctypes.c_int, ctypes.c_float],
+    "dpr_start": [_c_p, _c_p],
+    "dpr_request_free": [_c_p],
     "dpr_strerror": [ctypes.c_int],
     "dpr_last_cuda_error": [],
     "dpr_version": [],
@@ -230,6 +237,74 @@ def dpr_reduce_scatter_batch(inputs, K: int, M: int, N: Sequence[int], outputs,
                                         _MODES[mode], 1.0 / K if scale is None else scale,
                                         int(bool(accumulate)), _stream(stream))
     _check("dpr_reduce_scatter_batch", st)
+
+
+class Request:
+    """A persistent collective (dpr_*_init): the arguments were checked once;
+    start() enqueues the prepared kernel.  Keeps the bound tensors alive."""
+
+    def __init__(self, handle: int, keep: tuple):
+        self.handle = handle
+        self._keep = keep
+        self._start = lib().dpr_start
+
+    def start(self, stream=None) -> None:
+        st = self._start(self.handle, _stream(stream))
+        if st != 0:
+            raise DprError("dpr_start", st)
+
+    def close(self):
+        if self.handle:
+            h, self.handle = self.handle, None
+            _check("dpr_request_free", lib().dpr_request_free(h))
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def dpr_reduce_scatter_init(inputs, K: int, M: int, N: int, outputs, mode=RING_FP32,
+                            scale: float | None = None, accumulate: bool = False) -> Request:
+    """A persistent dpr_reduce_scatter (same arguments, without the stream)."""
+    chk = N > 0
+    ins = _rows(inputs, M * K, torch.bfloat16, N, "inputs", chk)
+    outs = _rows(outputs, K, torch.float32, N // K if K else 0, "outputs", chk)
+    h = ctypes.c_void_p()
+    st = lib().dpr_reduce_scatter_init(ctypes.byref(h), ins, K, M, N, outs, _MODES[mode],
+                                       1.0 / K if scale is None else scale, int(bool(accumulate)))
+    _check("dpr_reduce_scatter_init", st)
+    return Request(h.value, (inputs, outputs))
+
+
+def dpr_allgather_init(shards, K: int, N: int, outputs) -> Request:
+    """A persistent dpr_allgather (same arguments, without the stream)."""
+    chk = N > 0
+    sh = _rows(shards, K, torch.bfloat16, N // K if K else 0, "shards", chk)
+    outs = _rows(outputs, K, torch.bfloat16, N, "outputs", chk)
+    h = ctypes.c_void_p()
+    _check("dpr_allgather_init", lib().dpr_allgather_init(ctypes.byref(h), sh, K, N, outs))
+    return Request(h.value, (shards, outputs))
+
+
+def dpr_allreduce_init(inputs, K: int, N: int, outputs, mode=RING_FP32,
+                       scale: float | None = None) -> Request:
+    """A persistent dpr_allreduce (same arguments, without the stream)."""
+    chk = N > 0
+    ins = _rows(inputs, K, torch.bfloat16, N, "inputs", chk)
+    outs = _rows(outputs, K, torch.bfloat16, N, "outputs", chk)
+    h = ctypes.c_void_p()
+    st = lib().dpr_allreduce_init(ctypes.byref(h), ins, K, N, outs, _MODES[mode],
+                                  1.0 / K if scale is None else scale)
+    _check("dpr_allreduce_init", st)
+    return Request(h.value, (inputs, outputs))
 
 
 def dpr_set_programmatic_launch(enable: bool) -> bool:

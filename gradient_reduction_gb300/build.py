@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libdpr.so")
 SOURCES = ["dpr_api.cu", "reduce_kernels.cu", "gather_kernels.cu", "coalesced.cu",
-           "pipeline.cu", "cost_model.cpp", "flatten_noalloc.cu", "fragments.cu"]
+           "pipeline.cu", "cost_model.cpp", "flatten_noalloc.cu", "fragments.cu", "requests.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC,-O2",
          "-I", os.path.join(ROOT, "include")]

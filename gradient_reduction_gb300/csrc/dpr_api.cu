@@ -278,12 +278,50 @@ dpr_status dpr_cast_bf16_to_fp32(const void* in, float* out, int64_t n, void* st
 
 }  // extern "C"
 
-namespace {
+dpr_status dpr::prepare_allreduce(const void* const* in, int K, int64_t N, void* const* out,
+                                  int mode, float scale, ArParams* p, int* width_out) {
+    dpr_status st = check_kn(K, N);
+    if (st != DPR_OK) return st;
+    if (mode != DPR_SUM_RING_FP32 && mode != DPR_SUM_HOP_BF16) return DPR_ERR_INVALID_ARG;
+    if (N == 0) return DPR_OK;
+    if (!in || !out) return DPR_ERR_INVALID_ARG;
+    const int64_t S = N / K;
+    bool a16 = true, a32 = true;
+    std::vector<Span> outs;
+    for (int r = 0; r < K; ++r) {
+        if (!in[r] || !out[r]) return DPR_ERR_INVALID_ARG;
+        if (!aligned(in[r], 2) || !aligned(out[r], 2)) return DPR_ERR_ALIGNMENT;
+        a16 = a16 && aligned(in[r], 16) && aligned(out[r], 16);
+        a32 = a32 && aligned(in[r], 32) && aligned(out[r], 32);
+        outs.push_back(span_of(out[r], uint64_t(N) * 2));
+    }
+    const int width = access_width(S, a32, a16);
+    if (!pairwise_disjoint(outs)) return DPR_ERR_ALIAS;
+    for (int i = 0; i < K; ++i) {
+        const Span a = span_of(in[i], uint64_t(N) * 2);
+        for (int r = 0; r < K; ++r) {
+            if (i == r && in[i] == out[r]) continue;   // in place
+            if (overlaps(a, outs[r])) return DPR_ERR_ALIAS;
+        }
+    }
+    std::memset(p, 0, sizeof(*p));
+    for (int r = 0; r < K; ++r) {
+        p->in[r] = static_cast<const uint16_t*>(in[r]);
+        p->out[r] = static_cast<uint16_t*>(out[r]);
+    }
+    p->S = S;
+    p->su = width > 0 ? uint32_t(S / (2 * width)) : 0;
+    p->K = K;
+    p->scale = scale;
+    p->order = kAfterPrevious;
+    *width_out = width;
+    return DPR_OK;
+}
 
 // The checks of dpr_allgather, filling the parameter block and the access
 // width on success (nothing is launched).
-dpr_status prepare_allgather(const void* const* shard, int K, int64_t N, void* const* out,
-                             AgParams* p, int* width) {
+dpr_status dpr::prepare_allgather(const void* const* shard, int K, int64_t N, void* const* out,
+                                  AgParams* p, int* width) {
     dpr_status st = check_kn(K, N);
     if (st != DPR_OK) return st;
     if (N == 0) return DPR_OK;
@@ -323,8 +361,6 @@ dpr_status prepare_allgather(const void* const* shard, int K, int64_t N, void* c
     *width = access_width(S, a32, a16);
     return DPR_OK;
 }
-
-}  // namespace
 
 extern "C" {
 
@@ -381,40 +417,10 @@ dpr_status dpr_allgather_batch(int n, const void* const* shard, int K, const int
 
 dpr_status dpr_allreduce(const void* const* in, int K, int64_t N, void* const* out, int mode,
                          float scale, void* stream) {
-    dpr_status st = check_kn(K, N);
-    if (st != DPR_OK) return st;
-    if (mode != DPR_SUM_RING_FP32 && mode != DPR_SUM_HOP_BF16) return DPR_ERR_INVALID_ARG;
-    if (N == 0) return DPR_OK;
-    if (!in || !out) return DPR_ERR_INVALID_ARG;
-    const int64_t S = N / K;
-    bool a16 = true, a32 = true;
-    std::vector<Span> outs;
-    for (int r = 0; r < K; ++r) {
-        if (!in[r] || !out[r]) return DPR_ERR_INVALID_ARG;
-        if (!aligned(in[r], 2) || !aligned(out[r], 2)) return DPR_ERR_ALIGNMENT;
-        a16 = a16 && aligned(in[r], 16) && aligned(out[r], 16);
-        a32 = a32 && aligned(in[r], 32) && aligned(out[r], 32);
-        outs.push_back(span_of(out[r], uint64_t(N) * 2));
-    }
-    const int width = access_width(S, a32, a16);
-    if (!pairwise_disjoint(outs)) return DPR_ERR_ALIAS;
-    for (int i = 0; i < K; ++i) {
-        const Span a = span_of(in[i], uint64_t(N) * 2);
-        for (int r = 0; r < K; ++r) {
-            if (i == r && in[i] == out[r]) continue;   // in place
-            if (overlaps(a, outs[r])) return DPR_ERR_ALIAS;
-        }
-    }
     ArParams p;
-    std::memset(&p, 0, sizeof(p));
-    for (int r = 0; r < K; ++r) {
-        p.in[r] = static_cast<const uint16_t*>(in[r]);
-        p.out[r] = static_cast<uint16_t*>(out[r]);
-    }
-    p.S = S;
-    p.su = width > 0 ? uint32_t(S / (2 * width)) : 0;
-    p.K = K;
-    p.scale = scale;
+    int width = 0;
+    dpr_status st = prepare_allreduce(in, K, N, out, mode, scale, &p, &width);
+    if (st != DPR_OK || N == 0) return st;
     return cuda_status(launch_allreduce(p, mode, width, static_cast<cudaStream_t>(stream)));
 }
 

@@ -116,6 +116,13 @@ dpr_status prepare_reduce_scatter(const void* const* in, int K, int M, int64_t N
                                   float* const* out, int mode, float scale, int accumulate,
                                   RsParams* p, int* width);
 
+// The checks of dpr_allgather and dpr_allreduce, filling the parameter block
+// and the access width on success (nothing is launched).
+dpr_status prepare_allgather(const void* const* shard, int K, int64_t N, void* const* out,
+                             AgParams* p, int* width);
+dpr_status prepare_allreduce(const void* const* in, int K, int64_t N, void* const* out,
+                             int mode, float scale, ArParams* p, int* width);
+
 // dpr_reduce_scatter with a block budget (0 = the whole GPU); `programmatic`
 // as for launch_kernel.
 dpr_status reduce_scatter_capped(const void* const* in, int K, int M, int64_t N, float* const* out,

@@ -184,6 +184,39 @@ dpr_status dpr_allreduce(const void* const* in, int K, int64_t N, void* const* o
                          float scale, void* stream);
 
 /*
+ * Persistent collectives (after MPI-4's persistent collective operations,
+ * MPI_Allreduce_init / MPI_Start).  A ZeRO training loop reduces the same
+ * buckets into the same partitions at every step; these calls check the
+ * arguments and build the kernel's parameters once, so that each start costs
+ * one launch.
+ *
+ * dpr_reduce_scatter_init, dpr_allgather_init and dpr_allreduce_init take the
+ * arguments of dpr_reduce_scatter, dpr_allgather and dpr_allreduce (without
+ * the stream), check them exactly as those calls do, record the current
+ * device and return a request in *req (NULL on failure).  They allocate host
+ * memory only and make no other CUDA call.  The pointer arrays are read
+ * during the call; the buffers they point to must stay valid for as long as
+ * the request is started.
+ *
+ * dpr_start enqueues the prepared collective on `stream` (the device current
+ * at initialisation must be current; DPR_ERR_INVALID_ARG otherwise) with the
+ * same results and stream semantics as the one-shot call; a request built
+ * for N == 0 launches nothing.  dpr_request_free releases a request (NULL is
+ * a no-op); work already enqueued is unaffected.
+ */
+typedef struct dpr_request dpr_request;
+
+dpr_status dpr_reduce_scatter_init(dpr_request** req, const void* const* in, int K, int M,
+                                   int64_t N, float* const* out, int mode, float scale,
+                                   int accumulate);
+dpr_status dpr_allgather_init(dpr_request** req, const void* const* shard, int K, int64_t N,
+                              void* const* out);
+dpr_status dpr_allreduce_init(dpr_request** req, const void* const* in, int K, int64_t N,
+                              void* const* out, int mode, float scale);
+dpr_status dpr_start(const dpr_request* req, void* stream);
+dpr_status dpr_request_free(dpr_request* req);
+
+/*
  * Flat-bucket gather plan (the IPG bucket of ZeRO: DeepSpeed ZeRO-3 source
  * walkthrough, sections 3.2 and 5.1).  Gradient p of rank r occupies
  * elements [offset[p], offset[p] + numel[p]) of rank r's flat bucket.  In the

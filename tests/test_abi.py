@@ -35,7 +35,7 @@ def _declared():
 
 def test_exports_every_declared_function(L):
     names = _declared()
-    assert len(names) == 35
+    assert len(names) == 40
     for n in names:
         assert hasattr(L, n), n
 
@@ -352,3 +352,24 @@ def test_allgather_batch_rejections(L):
     assert ag(2, _arr(sh), K, n2, _arr(outs[:K] + [sh[0]] + outs[K + 1:]), None) == ALIAS
     # member 0 writes over member 1's shard
     assert ag(2, _arr(sh), K, n2, _arr([sh[K + 2] - 2 * S] + outs[1:]), None) == ALIAS
+
+
+def test_request_init_rejections(L):
+    """Persistent requests check their arguments as the one-shot calls do,
+    before any CUDA call; a refused init returns no request."""
+    K, N = 4, 64
+    ins, outs = _bufs(K, 1 << 20), _bufs(K, 1 << 20, BASE + (1 << 30))
+    h = ctypes.c_void_p(123)
+    assert L.dpr_reduce_scatter_init(ctypes.byref(h), _arr(ins), 1, 1, N, _arr(outs), 0, 1.0,
+                                     0) == INVALID
+    assert h.value is None
+    assert L.dpr_reduce_scatter_init(ctypes.byref(h), _arr(ins), K, 1, N,
+                                     _arr(outs[:3] + [ins[1] + 16]), 0, 1.0, 0) == ALIAS
+    assert L.dpr_reduce_scatter_init(None, _arr(ins), K, 1, N, _arr(outs), 0, 1.0, 0) == INVALID
+    assert L.dpr_allgather_init(ctypes.byref(h), _arr(ins), K, N + 2, _arr(outs)) == INVALID
+    assert L.dpr_allgather_init(ctypes.byref(h), _arr(ins), K, N,
+                                _arr(outs[:3] + [outs[3] + 1])) == ALIGN
+    assert L.dpr_allreduce_init(ctypes.byref(h), _arr(ins), K, N, _arr(outs), 5, 1.0) == INVALID
+    assert h.value is None
+    assert L.dpr_start(None, None) == INVALID
+    assert L.dpr_request_free(None) == OK
