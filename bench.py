@@ -69,28 +69,30 @@ BF16_KERNELS = ("rs_bf16_copy", "rs_bf16_add", "cast")
 # are not counted at either size, so the scaled write traffic is a slight
 # underestimate.
 NCU_TRAFFIC = {
-    "flatten": {"bytes": 16_313_106_432, "small_case_bytes": 1_019_569_152, "scale": 16,
-        "src_sha": "6474650912caab0c"},
-    "rs_fp32_m2": {"bytes": 19_156_946_944, "small_case_bytes": 1_197_309_184, "scale": 16,
-        "src_sha": "4675ad59026b5fb6"},
-    "rs_hop_m2_acc": {"bytes": 21_306_318_848, "small_case_bytes": 1_331_644_928, "scale": 16,
-        "src_sha": "4675ad59026b5fb6"},
-    "allgather": {"bytes": 8_733_552_640, "small_case_bytes": 545_847_040, "scale": 16,
-        "src_sha": "6474650912caab0c"},
-    "allreduce": {"bytes": 16_274_710_528, "small_case_bytes": 1_017_169_408, "scale": 16,
-        "src_sha": "4675ad59026b5fb6"},
-    "rs_fp32_m1": {"bytes": 10_438_463_488, "small_case_bytes": 652_403_968, "scale": 16,
-        "src_sha": "4675ad59026b5fb6"},
-    "rs_coalesced": {"bytes": 21_884_484_608, "small_case_bytes": 3_126_354_944, "scale": 7,
-        "src_sha": "7951d2db94cd0679"},
-    "ag_coalesced": {"bytes": 19_396_910_848, "small_case_bytes": 2_770_987_264, "scale": 7,
-        "src_sha": "05f53611035fac79"},
-    "rs_bf16_copy": {"bytes": 9_514_078_208, "small_case_bytes": 594_629_888, "scale": 16,
-        "src_sha": "4675ad59026b5fb6"},
-    "rs_bf16_add": {"bytes": 10_587_287_552, "small_case_bytes": 661_705_472, "scale": 16,
-        "src_sha": "4675ad59026b5fb6"},
-    "cast": {"bytes": 2_336_284_672, "small_case_bytes": 146_017_792, "scale": 16,
-        "src_sha": "d72896eb3f85bb94"},
+    "flatten": {"bytes": 16_296_275_968, "small_case_bytes": 1_018_517_248, "scale": 16,
+        "src_sha": "78b6341a823b0ac3"},
+    "rs_fp32_m2": {"bytes": 19_160_371_200, "small_case_bytes": 1_197_523_200, "scale": 16,
+        "src_sha": "8c6352237f5071d3"},
+    "rs_hop_m2_acc": {"bytes": 21_296_742_400, "small_case_bytes": 1_331_046_400, "scale": 16,
+        "src_sha": "8c6352237f5071d3"},
+    "allgather": {"bytes": 8_733_831_168, "small_case_bytes": 545_864_448, "scale": 16,
+        "src_sha": "78b6341a823b0ac3"},
+    "allreduce": {"bytes": 16_278_966_272, "small_case_bytes": 1_017_435_392, "scale": 16,
+        "src_sha": "8c6352237f5071d3"},
+    "rs_fp32_m1": {"bytes": 10_433_589_248, "small_case_bytes": 652_099_328, "scale": 16,
+        "src_sha": "8c6352237f5071d3"},
+    "rs_hop_m1": {"bytes": 10_435_891_200, "small_case_bytes": 652_243_200, "scale": 16,
+        "src_sha": "8c6352237f5071d3"},
+    "rs_coalesced": {"bytes": 21_889_134_848, "small_case_bytes": 3_127_019_264, "scale": 7,
+        "src_sha": "6f886be0ed469ddd"},
+    "ag_coalesced": {"bytes": 19_400_358_656, "small_case_bytes": 2_771_479_808, "scale": 7,
+        "src_sha": "a51ba914d18f42e6"},
+    "rs_bf16_copy": {"bytes": 9_526_312_960, "small_case_bytes": 595_394_560, "scale": 16,
+        "src_sha": "8c6352237f5071d3"},
+    "rs_bf16_add": {"bytes": 10_587_213_824, "small_case_bytes": 661_700_864, "scale": 16,
+        "src_sha": "8c6352237f5071d3"},
+    "cast": {"bytes": 2_331_516_928, "small_case_bytes": 145_719_808, "scale": 16,
+        "src_sha": "0d1bf71136293cc0"},
 }
 
 
