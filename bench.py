@@ -913,7 +913,8 @@ def run_sequence_bench(args):
         full = torch.empty(nb, K, N, dtype=bf, device=dev)
         full_l = [full[b] for b in range(nb)]
         # shard j of bucket b is chunk j of rank j's buffer: rows N + S elements apart
-        shards = [torch.as_strided(x[b], (K, S), (N + S, 1)) for b in range(nb)]
+        shards_all = torch.as_strided(x, (nb, K, S), (M * K * N, N + S, 1))
+        shards = [shards_all[b] for b in range(nb)]
     s.synchronize()
 
     def rs_single(key):
@@ -946,7 +947,7 @@ def run_sequence_bench(args):
             dpr.dpr_allgather(shards[b], K, N, full_l[b], stream=s)
 
     def ag_batch():
-        dpr.dpr_allgather_batch(shards, K, [N] * nb, full, stream=s)
+        dpr.dpr_allgather_batch(shards_all, K, [N] * nb, full, stream=s)
 
     def timed(fn):
         for _ in range(args.warmup):

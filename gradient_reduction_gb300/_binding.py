@@ -126,8 +126,16 @@ def _ptrs(ts: Sequence[torch.Tensor]):
     return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
 
 
+# The current stream's handle without building a torch.cuda.Stream object
+# (which costs a few microseconds per call); the public route serves when
+# this accessor is absent or CUDA is not initialised yet.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int:
     if stream is None:
+        if _raw_stream is not None and torch.cuda.is_initialized():
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
@@ -158,16 +166,18 @@ def _rows(x, count: int, dtype, n: int, what: str, check: bool = True):
         if not x.is_cuda or x.dtype != dtype:
             raise ValueError(f"{what}: need a CUDA {dtype} tensor")
         dev = torch.cuda.current_device()
-        if x.device.index != dev:
-            raise ValueError(f"{what}: tensor on cuda:{x.device.index}, current device is cuda:{dev}")
+        if x.get_device() != dev:
+            raise ValueError(f"{what}: tensor on cuda:{x.get_device()}, current device is cuda:{dev}")
         if x.dim() < 2 or x.shape[0] != count:
             raise ValueError(f"{what}: expected a tensor of {count} rows, got shape {tuple(x.shape)}")
-        if not _rows_contiguous(x):
+        if not (x.is_contiguous() or _rows_contiguous(x)):
             raise ValueError(f"{what}: every row must be contiguous")
         if x.numel() // max(count, 1) < n:
             raise ValueError(f"{what}: rows of {x.numel() // max(count, 1)} elements, need {n}")
     base, step = x.data_ptr(), x.stride(0) * x.element_size()
-    return (ctypes.c_void_p * count)(*[base + i * step for i in range(count)])
+    if step > 0:
+        return (ctypes.c_void_p * count)(*range(base, base + count * step, step))
+    return (ctypes.c_void_p * count)(*([base] * count))
 
 
 def _need(ts: Sequence[torch.Tensor], count: int, dtype, n: int, what: str):
@@ -179,9 +189,9 @@ def _need(ts: Sequence[torch.Tensor], count: int, dtype, n: int, what: str):
             raise ValueError(f"{what}: need contiguous CUDA {dtype} tensors")
         if dev is None:
             dev = torch.cuda.current_device()
-        if t.device.index != dev:
+        if t.get_device() != dev:
             # the kernels run on the current device and would fault on another's memory
-            raise ValueError(f"{what}: tensor on cuda:{t.device.index}, current device is cuda:{dev}")
+            raise ValueError(f"{what}: tensor on cuda:{t.get_device()}, current device is cuda:{dev}")
         if t.numel() < n:
             raise ValueError(f"{what}: tensor of {t.numel()} elements, need {n}")
 
@@ -204,15 +214,20 @@ def _member_rows(x, n: int, count: int, dtype, sizes: Sequence[int], what: str):
     """Pointers of n members' `count` buffers, member after member.  `x` is a
     sequence with one entry per member (each a sequence of tensors or one
     tensor of `count` rows), or one tensor [n, count, ...] whose rows are
-    contiguous, checked once."""
+    contiguous, checked once (its members may lie at any stride)."""
     if isinstance(x, torch.Tensor):
         if x.dim() < 3 or x.shape[0] != n or x.shape[1] != count:
             raise ValueError(f"{what}: expected a tensor of {n} members of {count} rows, "
                              f"got shape {tuple(x.shape)}")
-        if x.stride(0) != count * x.stride(1):
-            raise ValueError(f"{what}: members must be laid out back to back")
-        # merging the first two dimensions is a view, never a copy, given the strides
-        return _rows(x.flatten(0, 1), n * count, dtype, max(sizes, default=0), what)
+        if n == 0 or x.stride(0) == count * x.stride(1):
+            # merging the first two dimensions is a view, never a copy, given the strides
+            return _rows(x.flatten(0, 1), n * count, dtype, max(sizes, default=0), what)
+        # every member shares the first member's row layout: check that once
+        _rows(x[0], count, dtype, max(sizes, default=0), what)
+        es = x.element_size()
+        base, s0, s1 = x.data_ptr(), x.stride(0) * es, x.stride(1) * es
+        return (ctypes.c_void_p * (n * count))(
+            *[base + i * s0 + j * s1 for i in range(n) for j in range(count)])
     if len(x) != n:
         raise ValueError(f"{what}: need one entry per member")
     arrs = [_rows(x[i], count, dtype, sizes[i], f"{what}[{i}]", sizes[i] > 0) for i in range(n)]

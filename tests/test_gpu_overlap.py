@@ -328,7 +328,21 @@ def test_stacked_tensor_arguments_equal_lists():
     xb = x.unsqueeze(0).repeat(3, 1, 1)
     ob = torch.empty(3, K, S, device=dev)
     dpr.dpr_reduce_scatter_batch(xb, K, M, [N] * 3, ob, mode=ring.HOP_BF16)
+    # members whose rows cannot merge with the member dimension: shard j of
+    # member i is chunk j of rank j's buffer, rows N + S apart, members
+    # M*K*N apart; the batch must equal single calls given lists
+    sh3 = torch.as_strided(xb, (3, K, S), (M * K * N, N + S, 1))
+    fb = torch.empty(3, K, N, dtype=torch.bfloat16, device=dev)
+    dpr.dpr_allgather_batch(sh3, K, [N] * 3, fb)
+    fs = [torch.empty(K, N, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    for i in range(3):
+        dpr.dpr_allgather([sh3[i, j] for j in range(K)], K, N, list(fs[i].unbind(0)))
     torch.cuda.synchronize()
+    for i in range(3):
+        assert torch.equal(fb[i].view(torch.int16), fs[i].view(torch.int16)), i
+        want = torch.cat([xb[i, j, j * S:(j + 1) * S] for j in range(K)])
+        for r in range(K):
+            assert torch.equal(fb[i, r].view(torch.int16), want.view(torch.int16)), (i, r)
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
     assert torch.equal(full_a.view(torch.int16), full_b.view(torch.int16))
     for r in range(K):
