@@ -30,8 +30,8 @@ per-parameter path, the stream-overlapped bucket pipeline, the bf16
 partitions, configuration 5's sweep, configurations 1-4, the reduce-scatter
 straight from fragments, and one point chosen on the command line.
 
---impl reference times the CPU oracle (numpy, one process per host core, each
-on its own slab) on a bounded sample of the same workload.  With --gpus N > 1 (under torchrun) every rank runs an
+--impl reference times the CPU oracle (its C ring simulation, one process per
+host core, each on its own slab) on a bounded sample of the same workload.  With --gpus N > 1 (under torchrun) every rank runs an
 independent replica of the workload on its own GPU (the path does not shard
 across GPUs); the job value is the bytes of all ranks over the slowest rank's
 time.
@@ -1489,11 +1489,18 @@ class OracleSample:
         return cls(n_per_rank, {name: np.load(os.path.join(folder, name + ".npy"))
                                 for name in cls.ARRAYS})
 
-    def step(self):
-        from oracle import flatten as ofl
-        from oracle import ring
+    def step(self, impl: str = "numpy"):
+        """The five steps through the numpy simulation (oracle/ring.py,
+        oracle/flatten.py) or the C simulation (oracle/ring_sim.c)."""
+        if impl == "c":
+            from oracle import ring_c as ring
+            flatten_bucket = ring.flatten_bucket
+        else:
+            from oracle import flatten as ofl
+            from oracle import ring
+            flatten_bucket = ofl.flatten_bucket
         K, P, F, N = self.K, self.P, self.F, self.N
-        flat = ofl.flatten_bucket(self.frags, [F] * P, [p * F for p in range(P)], N)
+        flat = flatten_bucket(self.frags, [F] * P, [p * F for p in range(P)], N)
         x = self.ipg0 + flat
         ring.reduce_scatter(x, K, 2, ring.RING_FP32, 1.0 / K)
         ring.reduce_scatter(x, K, 2, ring.HOP_BF16, 1.0 / K, out_init=self.part)
@@ -1508,33 +1515,36 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def _slab_worker(folder, n, barrier, cmds):
+def _slab_worker(folder, n, barrier, cmds, impl):
     """One oracle process: every element position of the workload is
     independent, so each core runs the whole oracle on its own slab.  Waits at
     the barrier, runs the commanded number of passes, waits again."""
     smp = OracleSample.load(folder, n)
-    smp.step()                                  # warm-up
+    smp.step(impl)                              # warm-up
     while True:
         passes = cmds.get()
         if passes is None:
             return
         barrier.wait()
         for _ in range(passes):
-            smp.step()
+            smp.step(impl)
         barrier.wait()
 
 
 class OracleSlabPool:
     """`cores` spawned processes, each holding one slab (a K=8 sample of n
-    elements per rank) of the bench workload and running the oracle on it.
-    run(p) times p passes of every process, from a common start to the last
-    one's end.  Processes are started with spawn: none inherits the parent's
-    CUDA state."""
+    elements per rank) of the bench workload and running the oracle on it
+    (impl "numpy" or "c", one thread each).  run(p) times p passes of every
+    process, from a common start to the last one's end.  Processes are
+    started with spawn: none inherits the parent's CUDA state."""
 
-    def __init__(self, n: int, cores: int):
+    def __init__(self, n: int, cores: int, impl: str = "numpy"):
         import multiprocessing as mp
         ctx = mp.get_context("spawn")
-        self.n, self.cores = n, cores
+        self.n, self.cores, self.impl = n, cores, impl
+        if impl == "c":
+            from oracle import ring_c
+            ring_c.build()          # once, before the processes load it
         self.folder = tempfile.mkdtemp(prefix="oracle_slab_")
         smp = OracleSample(n)
         smp.save(self.folder)
@@ -1546,7 +1556,8 @@ class OracleSlabPool:
         os.environ["OMP_NUM_THREADS"] = "1"     # one thread per process
         try:
             self.procs = [ctx.Process(target=_slab_worker,
-                                      args=(self.folder, n, self.barrier, q), daemon=True)
+                                      args=(self.folder, n, self.barrier, q, impl),
+                                      daemon=True)
                           for q in self.cmds]
             for pr in self.procs:
                 pr.start()
@@ -1586,28 +1597,38 @@ def time_oracle(n_per_rank: int, min_seconds: float, min_steps: int = 1):
     return smp, steps, el
 
 
-def cpu_baseline(args):
-    """The oracle on every host core (one slab per process), with the
-    single-thread figure beside it."""
-    n = 1 << 20
-    smp, steps1, el1 = time_oracle(n, args.cpu_seconds / 2)
-    one = smp.bytes * steps1 / el1 / 1e9
-    del smp
-    cores = host_cores()
-    pool = OracleSlabPool(n, cores)
+def time_pool(n: int, cores: int, impl: str, seconds: float):
+    """GB/s of `cores` slab processes running the oracle `impl` for about
+    `seconds`, with the passes and the time taken."""
+    pool = OracleSlabPool(n, cores, impl)
     try:
         t1 = pool.run(1)
-        passes = max(1, round(args.cpu_seconds / 2 / t1))
+        passes = max(1, round(seconds / t1))
         el = pool.run(passes)
     finally:
         pool.close()
-    value = pool.bytes * cores * passes / el / 1e9
+    return pool.bytes * cores * passes / el / 1e9, passes, el
+
+
+def cpu_baseline(args):
+    """The oracle on every host core, one slab per process: the C simulation
+    (the line's value) and the numpy simulation, with the numpy single-process
+    figure beside them."""
+    n = 1 << 20
+    smp, steps1, el1 = time_oracle(n, args.cpu_seconds / 3)
+    one = smp.bytes * steps1 / el1 / 1e9
+    del smp
+    cores = host_cores()
+    value, passes, el = time_pool(n, cores, "c", args.cpu_seconds / 3)
+    np_value, np_passes, np_el = time_pool(n, cores, "numpy", args.cpu_seconds / 3)
     return {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "single_core_value": round(one, 4),
+            "oracle": "C ring simulation (oracle/ring_sim.c, -O2, one thread per process)",
+            "numpy_value": round(np_value, 4), "numpy_single_core_value": round(one, 4),
             "sample": f"K=8, the same five steps; {cores} processes, each running the oracle "
-                      f"(numpy, one thread) on its own slab of {n} elements per rank (32 "
-                      f"fragments of {n // 32}), {passes} passes in {el:.1f} s; one process "
-                      f"alone: {steps1} passes in {el1:.1f} s"}
+                      f"on its own slab of {n} elements per rank (32 fragments of {n // 32}): "
+                      f"C simulation {passes} passes in {el:.1f} s, numpy simulation "
+                      f"{np_passes} passes in {np_el:.1f} s; one numpy process alone: "
+                      f"{steps1} passes in {el1:.1f} s"}
 
 
 def common_config(world):
@@ -1620,14 +1641,14 @@ def common_config(world):
 
 
 def run_reference(args):
-    """The reference arm: the oracle on every host core, one slab per process,
-    each step one pass of every process over its slab."""
+    """The reference arm: the oracle (the C simulation) on every host core,
+    one slab per process, each step one pass of every process over its slab."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     n = 1 << 20          # per process, as in the CPU baseline of the bench line
     cores = host_cores()
-    pool = OracleSlabPool(n, cores)
+    pool = OracleSlabPool(n, cores, "c")
     try:
         for _ in range(args.warmup):
             pool.run(1)
@@ -1643,9 +1664,11 @@ def run_reference(args):
         "data": "synthetic (seeded counter-hash generator; Box-Muller normals, uniform parameters)",
         "config": common_config(1),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "oracle": "C ring simulation (oracle/ring_sim.c, -O2, one thread "
+                                   "per process)",
                          "sample": f"K=8, the same five steps per step; {cores} processes, each "
-                                   f"running the oracle (numpy, one thread) on its own slab of "
-                                   f"{n} elements per rank (32 fragments of {n // 32})"},
+                                   f"running the oracle (C simulation, one thread) on its own "
+                                   f"slab of {n} elements per rank (32 fragments of {n // 32})"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
