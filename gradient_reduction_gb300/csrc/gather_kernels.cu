@@ -19,6 +19,31 @@ namespace {
 // K-1 blocks from L2.  Every block then writes a single contiguous stream.
 // In the in-place form (shard j inside replica j) the block for r == j has
 // nothing to do, so no block writes memory that another block reads.
+// The replica stores carry an L2 evict-first policy: the K-1 other blocks of
+// a tile read the shard tile from L2, and marking the written replica lines as
+// the first to leave keeps those shard tiles resident.  Measured on GB300 at
+// K=8, 1 GiB per rank: 0.45% faster than plain stores (7032 against 7000
+// GB/s), bit-identical; the same policy on a plain copy changed nothing.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+template <int W>
+__device__ __forceinline__ void store_words_ef(uint16_t* p, const uint32_t (&w)[W], uint64_t pol) {
+    if constexpr (W == 8) {
+        asm volatile("st.global.L2::cache_hint.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+                     ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                       "r"(w[6]), "r"(w[7]), "l"(pol)
+                     : "memory");
+    } else {
+        asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
+                     ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "l"(pol)
+                     : "memory");
+    }
+}
+
 // Copies the tile of block b (one tile of shard j into replica r).
 template <int W>
 __device__ __forceinline__ void ag_tile(const AgParams& p, uint64_t b) {
@@ -31,6 +56,7 @@ __device__ __forceinline__ void ag_tile(const AgParams& p, uint64_t b) {
     const uint64_t n = (S - t0 < uint64_t(kAgTile)) ? S - t0 : uint64_t(kAgTile);
     const uint16_t* src = p.shard[j] + t0;
     uint16_t* dst = p.out[r] + j * S + t0;
+    const uint64_t pol = evict_first_policy();
     constexpr int E = 2 * W;
     if (n == uint64_t(kAgTile)) {             // full tile: no per-unit guard
 #pragma unroll
@@ -38,7 +64,7 @@ __device__ __forceinline__ void ag_tile(const AgParams& p, uint64_t b) {
             const int i = (u * kThreads + int(threadIdx.x)) * E;
             uint32_t w[W];
             load_words<W, true>(src + i, w);
-            store_words<W>(dst + i, w);
+            store_words_ef<W>(dst + i, w, pol);
         }
         return;
     }
@@ -48,7 +74,7 @@ __device__ __forceinline__ void ag_tile(const AgParams& p, uint64_t b) {
         if (i < n) {
             uint32_t w[W];
             load_words<W, true>(src + i, w);
-            store_words<W>(dst + i, w);
+            store_words_ef<W>(dst + i, w, pol);
         }
     }
 }
