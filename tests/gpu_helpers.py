@@ -1,5 +1,6 @@
 """Shared pieces of the GPU parity tests: device buffers from the seeded
-generator, and the oracle evaluated on sampled element positions.
+generator, the oracle evaluated on sampled element positions, and every
+element of a reduce-scatter against the oracle's C ring simulation.
 
 A reduce-scatter's result at position t of chunk j depends only on the K (x M)
 inputs at element j*S + t and on j (which fixes the ring order).  So the
@@ -13,6 +14,7 @@ import pytest
 import torch
 
 from oracle import ring
+from oracle import ring_c
 from workloads import synthetic as syn
 
 MODES = (ring.RING_FP32, ring.HOP_BF16)
@@ -141,3 +143,14 @@ class Arena:
             free[off + e0 * es: off + (e0 + n) * es] = False
         bad = np.flatnonzero(free & (after != self.before))
         assert bad.size == 0, f"{bad.size} bytes outside the written regions changed, first at {bad[0]}"
+
+
+def assert_rs_every_element(x, out, K: int, M: int, mode: int, scale: float, what=""):
+    """Every element of a reduce-scatter's K fp32 shards against the oracle's C
+    ring simulation run on the same inputs, copied from the device (x[m*K + r]
+    bf16 of N, out[j] fp32 of N/K)."""
+    torch.cuda.synchronize()
+    host_x = [bits(t) for t in x]
+    want, _ = ring_c.reduce_scatter(host_x, K, M, mode, scale)
+    for j in range(K):
+        assert_f32_equal(out[j].cpu().numpy(), want[j], f"{what} shard {j}")

@@ -2,8 +2,11 @@
 
 Results are compared with the oracle on sampled positions of every chunk (the
 first, last and random positions; the oracle runs the same ring on those
-positions of every rank), and checked over every element with properties
-that hold at any size: the reduce-scatter's error bound against the exact
+positions of every rank); the reduce-scatters of configurations 2 and 3 (56
+tensors), and of every sweep point with at most 2 GiB of inputs, also at every
+element, against the oracle's C ring simulation on the inputs copied back from
+the device.  Every element is also checked with
+properties that hold at any size: the reduce-scatter's error bound against the exact
 fp64 sum, all-gather replicas identical to the concatenated shards, flat
 buckets identical to the concatenated gradients.  Inputs are generated on the
 GPU by the seeded generator; the tests also check that the device-generated
@@ -84,6 +87,8 @@ def test_cfg2_reduce_scatter(mode):
     T = _check_rs_sampled(out, cfg.at, K, 1, S, mode, 1.0 / K, seed=2 + mode)
     _check_device_inputs(x, cfg.at, K, 1, S, T)
     _rs_error_bound(x, out, K, 1, S, mode)
+    # every element, against the C ring simulation on the same 400 MB of inputs
+    H.assert_rs_every_element(x, out, K, 1, mode, 1.0 / K, "cfg2")
 
 
 # ---- config 3: fragmented transformer gradients, flatten + reduce-scatter -----------
@@ -104,7 +109,7 @@ def _bucket_at_fn(cfg, bk):
     return at
 
 
-def _run_cfg3(cfg, mode, check_buckets):
+def _run_cfg3(cfg, mode, check_buckets, every_element=False):
     dev = H.device()
     K = cfg.K
     arr = cfg.arrival_order()
@@ -137,6 +142,10 @@ def _run_cfg3(cfg, mode, check_buckets):
             torch.cuda.synchronize()
             _check_rs_sampled(out, _bucket_at_fn(cfg, b), K, 1, S, mode, 1.0 / K,
                               seed=bi, w=32)
+        if every_element:
+            # the whole bucket, against the C ring simulation on the gathered
+            # bucket (equal to the gradients laid end to end, checked above)
+            H.assert_rs_every_element(views, out, K, 1, mode, 1.0 / K, f"bucket {bi}")
         shard_off += S
     torch.cuda.synchronize()
     for p in plans:
@@ -147,7 +156,7 @@ def _run_cfg3(cfg, mode, check_buckets):
 
 @pytest.mark.parametrize("mode", H.MODES)
 def test_cfg3_flatten_reduce_scatter_56_tensors(mode):
-    _run_cfg3(C.CFG3, mode, check_buckets={0, 1, 2, 5, 20, 41})
+    _run_cfg3(C.CFG3, mode, check_buckets={0, 1, 2, 5, 20, 41}, every_element=True)
 
 
 def test_cfg3_flatten_reduce_scatter_224_tensors():
@@ -191,10 +200,13 @@ def _sweep_point(K, nbytes, dev, check_ag_ar):
     out = [torch.empty(S, dtype=torch.float32, device=dev) for _ in range(K)]
     T = H.sample_positions(S, 16, K + nbytes)
     xh = H.gather_inputs(cfg.at, K, M, S, T)
+    every = M * K * nbytes <= (2 << 30)      # inputs the host oracle takes whole
     for mode in H.MODES:
         dpr.dpr_reduce_scatter(x, K, M, N, out, mode=mode, scale=1.0 / K)
         torch.cuda.synchronize()
         _check_rs_sampled(out, cfg.at, K, M, S, mode, 1.0 / K, seed=K + nbytes, w=16, x=xh)
+        if every:
+            H.assert_rs_every_element(x, out, K, M, mode, 1.0 / K, f"K={K} {nbytes} B")
     _check_device_inputs(x, cfg.at, K, M, S, T)
     if check_ag_ar:
         ar = [torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(K)]
