@@ -69,30 +69,30 @@ BF16_KERNELS = ("rs_bf16_copy", "rs_bf16_add", "cast")
 # are not counted at either size, so the scaled write traffic is a slight
 # underestimate.
 NCU_TRAFFIC = {
-    "flatten": {"bytes": 16_310_562_816, "small_case_bytes": 1_019_410_176, "scale": 16,
-        "src_sha": "2a93e8d326850655"},
-    "rs_fp32_m2": {"bytes": 19_160_371_200, "small_case_bytes": 1_197_523_200, "scale": 16,
-        "src_sha": "8c6352237f5071d3"},
-    "rs_hop_m2_acc": {"bytes": 21_296_742_400, "small_case_bytes": 1_331_046_400, "scale": 16,
-        "src_sha": "8c6352237f5071d3"},
-    "allgather": {"bytes": 8_726_077_440, "small_case_bytes": 545_379_840, "scale": 16,
-        "src_sha": "2a93e8d326850655"},
-    "allreduce": {"bytes": 16_278_966_272, "small_case_bytes": 1_017_435_392, "scale": 16,
-        "src_sha": "8c6352237f5071d3"},
-    "rs_fp32_m1": {"bytes": 10_433_589_248, "small_case_bytes": 652_099_328, "scale": 16,
-        "src_sha": "8c6352237f5071d3"},
-    "rs_hop_m1": {"bytes": 10_435_891_200, "small_case_bytes": 652_243_200, "scale": 16,
-        "src_sha": "8c6352237f5071d3"},
-    "rs_coalesced": {"bytes": 21_889_134_848, "small_case_bytes": 3_127_019_264, "scale": 7,
-        "src_sha": "6f886be0ed469ddd"},
-    "ag_coalesced": {"bytes": 19_400_358_656, "small_case_bytes": 2_771_479_808, "scale": 7,
-        "src_sha": "a51ba914d18f42e6"},
-    "rs_bf16_copy": {"bytes": 9_526_312_960, "small_case_bytes": 595_394_560, "scale": 16,
-        "src_sha": "8c6352237f5071d3"},
-    "rs_bf16_add": {"bytes": 10_587_213_824, "small_case_bytes": 661_700_864, "scale": 16,
-        "src_sha": "8c6352237f5071d3"},
-    "cast": {"bytes": 2_331_516_928, "small_case_bytes": 145_719_808, "scale": 16,
-        "src_sha": "0d1bf71136293cc0"},
+    "flatten": {"bytes": 16_290_209_792, "small_case_bytes": 1_018_138_112, "scale": 16,
+        "src_sha": "578139312553fd43"},
+    "rs_fp32_m2": {"bytes": 19_163_496_448, "small_case_bytes": 1_197_718_528, "scale": 16,
+        "src_sha": "bf44fabf80dea9cc"},
+    "rs_hop_m2_acc": {"bytes": 21_305_192_448, "small_case_bytes": 1_331_574_528, "scale": 16,
+        "src_sha": "bf44fabf80dea9cc"},
+    "allgather": {"bytes": 8_736_522_240, "small_case_bytes": 546_032_640, "scale": 16,
+        "src_sha": "578139312553fd43"},
+    "allreduce": {"bytes": 16_272_740_352, "small_case_bytes": 1_017_046_272, "scale": 16,
+        "src_sha": "bf44fabf80dea9cc"},
+    "rs_fp32_m1": {"bytes": 10_433_806_336, "small_case_bytes": 652_112_896, "scale": 16,
+        "src_sha": "bf44fabf80dea9cc"},
+    "rs_hop_m1": {"bytes": 10_429_546_496, "small_case_bytes": 651_846_656, "scale": 16,
+        "src_sha": "bf44fabf80dea9cc"},
+    "rs_coalesced": {"bytes": 21_887_973_632, "small_case_bytes": 3_126_853_376, "scale": 7,
+        "src_sha": "73cc97b61fdb9af0"},
+    "ag_coalesced": {"bytes": 19_398_374_912, "small_case_bytes": 2_771_196_416, "scale": 7,
+        "src_sha": "5938d73fd6467d76"},
+    "rs_bf16_copy": {"bytes": 9_522_950_144, "small_case_bytes": 595_184_384, "scale": 16,
+        "src_sha": "bf44fabf80dea9cc"},
+    "rs_bf16_add": {"bytes": 10_583_232_512, "small_case_bytes": 661_452_032, "scale": 16,
+        "src_sha": "bf44fabf80dea9cc"},
+    "cast": {"bytes": 2_331_922_432, "small_case_bytes": 145_745_152, "scale": 16,
+        "src_sha": "f16c6d4024820bfc"},
 }
 
 

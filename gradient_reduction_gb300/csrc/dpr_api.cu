@@ -135,7 +135,8 @@ dpr_status dpr::prepare_reduce_scatter(const void* const* in, int K, int M, int6
         a32 = a32 && aligned(out[j], 32);
         outs.push_back(span_of(out[j], uint64_t(S) * 4));
     }
-    const int width = access_width(S, a32, a16);
+    const bool edge = edge_unit(S, K, a32, false);
+    const int width = edge ? 8 : access_width(S, a32, a16);
     if (!pairwise_disjoint(outs)) return DPR_ERR_ALIAS;
     for (int i = 0; i < M * K; ++i) {
         const Span a = span_of(in[i], uint64_t(N) * 2);
@@ -146,7 +147,8 @@ dpr_status dpr::prepare_reduce_scatter(const void* const* in, int K, int M, int6
     for (int i = 0; i < M * K; ++i) p->in[i] = static_cast<const uint16_t*>(in[i]);
     for (int j = 0; j < K; ++j) p->out[j] = out[j];
     p->S = S;
-    p->su = width > 0 ? uint32_t(S / (2 * width)) : 0;
+    p->su = chunk_units(S, width, edge);
+    p->edge = edge ? 1 : 0;
     p->K = K;
     p->M = M;
     p->scale = scale;
@@ -295,22 +297,29 @@ dpr_status dpr::prepare_allreduce(const void* const* in, int K, int64_t N, void*
         a32 = a32 && aligned(in[r], 32) && aligned(out[r], 32);
         outs.push_back(span_of(out[r], uint64_t(N) * 2));
     }
-    const int width = access_width(S, a32, a16);
+    bool in_place = false;
     if (!pairwise_disjoint(outs)) return DPR_ERR_ALIAS;
     for (int i = 0; i < K; ++i) {
         const Span a = span_of(in[i], uint64_t(N) * 2);
         for (int r = 0; r < K; ++r) {
-            if (i == r && in[i] == out[r]) continue;   // in place
+            if (i == r && in[i] == out[r]) {           // in place
+                in_place = true;
+                continue;
+            }
             if (overlaps(a, outs[r])) return DPR_ERR_ALIAS;
         }
     }
+    // the edge unit reads 8 elements of a neighbouring chunk: never over outputs
+    const bool edge = !in_place && edge_unit(S, K, a32, true);
+    const int width = edge ? 8 : access_width(S, a32, a16);
     std::memset(p, 0, sizeof(*p));
     for (int r = 0; r < K; ++r) {
         p->in[r] = static_cast<const uint16_t*>(in[r]);
         p->out[r] = static_cast<uint16_t*>(out[r]);
     }
     p->S = S;
-    p->su = width > 0 ? uint32_t(S / (2 * width)) : 0;
+    p->su = chunk_units(S, width, edge);
+    p->edge = edge ? 1 : 0;
     p->K = K;
     p->scale = scale;
     p->order = kAfterPrevious;

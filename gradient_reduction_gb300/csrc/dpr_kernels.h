@@ -33,12 +33,13 @@ struct RsParams {
     const uint16_t* in[DPR_MAX_MICRO * DPR_MAX_RANKS];  // in[m*K + r]
     float* out[DPR_MAX_RANKS];                          // partition shard j
     int64_t S;          // elements per chunk
-    uint32_t su;        // 2*width-element units per chunk (vector kernels)
+    uint32_t su;        // 2*width-element units per chunk (vector kernels), edge unit included
     int K;
     int M;
     float scale;
     int accumulate;
     int order;          // kAfterPrevious / kBesidePrevious
+    int edge;           // see edge_unit(): width 8 with one 8-element unit per chunk
 };
 
 struct ArParams {
@@ -49,6 +50,7 @@ struct ArParams {
     int K;
     float scale;
     int order;
+    int edge;
 };
 
 struct AgParams {
@@ -91,6 +93,34 @@ inline int access_width(int64_t S, bool aligned32, bool aligned16) {
     if (aligned32 && S % 16 == 0) return 8;
     if (aligned16 && S % 8 == 0) return 4;
     return 0;
+}
+
+// The reduce-scatter and all-reduce also take 32-byte accesses when every
+// buffer is 32-byte aligned, S % 16 == 8, the chunk is long (S >=
+// kEdgeMinChunk) and the layout is built for K (below, all even); the
+// all-reduce only out of place.  Chunk j then starts 8 elements past a
+// 32-byte boundary when j is odd.  Its 32-byte units start at the first
+// boundary, and one more unit, a 32-byte window reaching 8 elements into the
+// neighbouring chunk, covers the 8 elements left over: the head of an odd
+// chunk, the tail of an even one (K even: every even chunk has a chunk after
+// it).  The unit count per chunk is (S - 8) / 16 + 1.
+// Measured on GB300 at K = 8 (isolated launches): 5-8% faster than 16-byte
+// accesses from S = 4.2M elements up, equal at 3.7M, 3-5% slower at 3.1M and
+// 2.1M (shorter launches gain from the 16-byte kernel's finer blocks), so
+// shorter chunks keep 16-byte accesses.
+// The layout is built for the reduce-scatter at K = 2, 4, 8, 16, 32 and the
+// all-reduce at K = 2, 4, 8: there it fits 64 registers without spilling.
+constexpr int64_t kEdgeMinChunk = int64_t(1) << 22;
+inline bool edge_unit(int64_t S, int K, bool aligned32, bool allreduce) {
+    const bool built = allreduce ? (K == 2 || K == 4 || K == 8)
+                                 : (K == 2 || K == 4 || K == 8 || K == 16 || K == 32);
+    return built && aligned32 && S % 16 == 8 && S >= kEdgeMinChunk;
+}
+
+// Units per chunk of the vector kernels for `width` (and the edge layout).
+inline uint32_t chunk_units(int64_t S, int width, bool edge) {
+    if (width <= 0) return 0;
+    return edge ? uint32_t((S - 8) / 16 + 1) : uint32_t(S / (2 * width));
 }
 
 // Launches `kernel` (kThreads threads per block) on `s` with the parameter

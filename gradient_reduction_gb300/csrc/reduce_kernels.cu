@@ -13,10 +13,12 @@
 //
 // Layout: grid.y = chunk j (so the ring's start rank is uniform per block);
 // each thread owns one unit of 2W consecutive elements of its chunk (W = 8:
-// 32-byte accesses, W = 4: 16-byte accesses), and there are as many blocks
-// as units / 256 -- on GB300 this keeps more requests in flight than a
-// persistent grid and streams HBM faster.  Element-wise kernels serve layouts
-// that are not 16-byte aligned or chunks that are not a multiple of 8.
+// 32-byte accesses, W = 4: 16-byte accesses; with W = 8 a chunk whose length
+// is 8 more than a multiple of 16 has one 8-element unit at its unaligned
+// end), and there are as many blocks as units / 256 -- on GB300 this keeps
+// more requests in flight than a persistent grid and streams HBM faster.
+// Element-wise kernels serve layouts that are not 16-byte aligned or chunks
+// that are not a multiple of 8.
 #include "dpr_device.cuh"
 #include "dpr_kernels.h"
 #include "dpr_ring.cuh"
@@ -29,19 +31,66 @@ namespace {
 // One unit per thread when the grid covers the chunk (the default launch);
 // with a capped grid (a block budget, e.g. to leave SMs to concurrent
 // compute) the same blocks stride over the remaining units.
-template <int KC, int M, int MODE, int W>
-__global__ void __launch_bounds__(kThreads) rs_vec(const __grid_constant__ RsParams p) {
+//
+// EDGE (rs_vec_edge; p.edge, see edge_unit(): S % 16 == 8, 32-byte aligned
+// buffers, K even): chunk j starts 8 elements past a 32-byte boundary when j
+// is odd, so its 32-byte units start 8 elements in, and the chunk's last unit
+// is a 32-byte window around the 8 elements left over -- the head of an odd
+// chunk, [c0 - 8, c0 + 8), or the tail of an even one, [c0 + S - 8,
+// c0 + S + 8).  The window's other 8 elements belong to the neighbouring
+// chunk, inside the buffer (an odd chunk has a chunk before it; with K even
+// an even chunk has one after it); the inputs are read-only here, those 8
+// sums are dropped and only the chunk's own 8 are stored.  The edge unit thus
+// runs the same 32-byte code as every other unit.  The kernel is capped at 64
+// registers (4 blocks per SM); for the K it is built for it does not spill.
+template <int KC, int M, int MODE, int W, bool EDGE>
+__device__ __forceinline__ void rs_units(const RsParams& p) {
+    static_assert(!EDGE || W == 8, "the edge layout has 32-byte units");
     const int j = blockIdx.y;
     order_start(p.order);
     order_enter(p.order);
-    for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < p.su;
-         t += uint64_t(gridDim.x) * kThreads) {
-        const uint64_t e = uint64_t(j) * uint64_t(p.S) + uint64_t(2 * W) * t;
-        float acc[2 * W];
-        ring_sum<KC, M, MODE, W, true>(p.in, p.K, j, e, acc);
-        store_shard<W>(p.out[j] + uint64_t(2 * W) * t, acc, p.scale, p.accumulate);
+    if constexpr (EDGE) {
+        const uint64_t c0 = uint64_t(j) * uint64_t(p.S);
+        const bool odd = (c0 & 15) != 0;
+        const uint64_t body = uint64_t(p.su) - 1;
+        for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < p.su;
+             t += uint64_t(gridDim.x) * kThreads) {
+            const bool edge = t == body;
+            // one summation per unit (a second call site would double the registers)
+            const uint64_t win = edge ? (odd ? c0 - 8 : c0 + uint64_t(p.S) - 8)
+                                      : c0 + (odd ? 8 : 0) + 16 * t;
+            float acc[16];
+            ring_sum<KC, M, MODE, 8, true>(p.in, p.K, j, win, acc);
+            if (edge) {
+                float mine[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mine[k] = odd ? acc[8 + k] : acc[k];
+                store_shard<4>(p.out[j] + (odd ? 0 : uint64_t(p.S) - 8), mine, p.scale,
+                               p.accumulate);
+            } else {
+                store_shard<8>(p.out[j] + (win - c0), acc, p.scale, p.accumulate);
+            }
+        }
+    } else {
+        for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < p.su;
+             t += uint64_t(gridDim.x) * kThreads) {
+            const uint64_t e = uint64_t(j) * uint64_t(p.S) + uint64_t(2 * W) * t;
+            float acc[2 * W];
+            ring_sum<KC, M, MODE, W, true>(p.in, p.K, j, e, acc);
+            store_shard<W>(p.out[j] + uint64_t(2 * W) * t, acc, p.scale, p.accumulate);
+        }
     }
     order_exit(p.order);
+}
+
+template <int KC, int M, int MODE, int W>
+__global__ void __launch_bounds__(kThreads) rs_vec(const __grid_constant__ RsParams p) {
+    rs_units<KC, M, MODE, W, false>(p);
+}
+
+template <int KC, int M, int MODE>
+__global__ void __launch_bounds__(kThreads, 4) rs_vec_edge(const __grid_constant__ RsParams p) {
+    rs_units<KC, M, MODE, 8, true>(p);
 }
 
 // bf16 partition shards (the ZeRO-3 partition buffer): the shard is rounded
@@ -166,14 +215,50 @@ __global__ void __launch_bounds__(kThreads) rs_scalar(const __grid_constant__ Rs
 // Inputs may be the outputs (in place): each thread reads all K addends of
 // its elements before writing them, no other thread touches those elements,
 // and the loads use the coherent path.
-template <int KC, int MODE, int W>
-__global__ void __launch_bounds__(kThreads) ar_vec(const __grid_constant__ ArParams p) {
+// The all-reduce of 16 elements from e: ring sum, scale, bf16.
+template <int KC, int MODE>
+__device__ __forceinline__ void ar_words(const ArParams& p, int K, int j, uint64_t e,
+                                         uint32_t (&w)[8]) {
+    float acc[16];
+    ring_sum<KC, 1, MODE, 8, false>(p.in, K, j, e, acc);
+    const float s = p.scale;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = pack_bf16x2(__fmul_rn(acc[2 * k], s), __fmul_rn(acc[2 * k + 1], s));
+}
+
+// EDGE as in rs_vec, for out-of-place calls only (an in-place call writes the
+// inputs, so no unit may read a neighbouring chunk's elements): the window's
+// own 8 elements are stored, with 16-byte stores.
+template <int KC, int MODE, int W, bool EDGE>
+__device__ __forceinline__ void ar_units(const ArParams& p) {
+    static_assert(!EDGE || W == 8, "the edge layout has 32-byte units");
     order_enter(p.order);
     const uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x;
     if (t >= p.su) return;
     const int j = blockIdx.y;
     const int K = KC > 0 ? KC : p.K;
-    const uint64_t e = uint64_t(j) * uint64_t(p.S) + uint64_t(2 * W) * t;
+    const uint64_t c0 = uint64_t(j) * uint64_t(p.S);
+    if constexpr (EDGE) {
+        const bool odd = (c0 & 15) != 0;
+        const bool edge = t + 1 == uint64_t(p.su);
+        const uint64_t win = edge ? (odd ? c0 - 8 : c0 + uint64_t(p.S) - 8)
+                                  : c0 + (odd ? 8 : 0) + 16 * t;
+        uint32_t w[8];
+        ar_words<KC, MODE>(p, K, j, win, w);
+        if (edge) {
+            uint32_t mine[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mine[k] = odd ? w[4 + k] : w[k];
+            const uint64_t e = odd ? c0 : c0 + uint64_t(p.S) - 8;
+#pragma unroll 8
+            for (int r = 0; r < K; ++r) store_words<4>(p.out[r] + e, mine);
+            return;
+        }
+#pragma unroll 8
+        for (int r = 0; r < K; ++r) store_words<8>(p.out[r] + win, w);
+        return;
+    }
+    const uint64_t e = c0 + uint64_t(2 * W) * t;
     float acc[2 * W];
     ring_sum<KC, 1, MODE, W, false>(p.in, K, j, e, acc);
     const float s = p.scale;
@@ -182,6 +267,16 @@ __global__ void __launch_bounds__(kThreads) ar_vec(const __grid_constant__ ArPar
     for (int k = 0; k < W; ++k) w[k] = pack_bf16x2(__fmul_rn(acc[2 * k], s), __fmul_rn(acc[2 * k + 1], s));
 #pragma unroll 8
     for (int r = 0; r < K; ++r) store_words<W>(p.out[r] + e, w);
+}
+
+template <int KC, int MODE, int W>
+__global__ void __launch_bounds__(kThreads) ar_vec(const __grid_constant__ ArParams p) {
+    ar_units<KC, MODE, W, false>(p);
+}
+
+template <int KC, int MODE>
+__global__ void __launch_bounds__(kThreads, 4) ar_vec_edge(const __grid_constant__ ArParams p) {
+    ar_units<KC, MODE, 8, true>(p);
 }
 
 template <int MODE>
@@ -208,8 +303,8 @@ __global__ void __launch_bounds__(kThreads) ar_scalar(const __grid_constant__ Ar
 }
 
 // The vector kernels are specialised for the configured K (both access
-// widths: 16-byte accesses serve chunks whose length is a multiple of 8 but
-// not 16, such as 25,000,000 / 8); other K use the run-time-K form.
+// widths: 16-byte accesses serve buffers that are 16- but not 32-byte
+// aligned); other K use the run-time-K form.
 template <int M, int MODE, int W>
 const void* rs_vec_for(int K) {
     switch (K) {
@@ -223,8 +318,23 @@ const void* rs_vec_for(int K) {
     }
 }
 
+// The edge layout exists for the K that edge_unit() admits for the
+// reduce-scatter (2-32); other K never set RsParams::edge.
 template <int M, int MODE>
-const void* rs_kernel_for(int K, int W) {
+const void* rs_edge_for(int K) {
+    switch (K) {
+        case 2: return reinterpret_cast<const void*>(rs_vec_edge<2, M, MODE>);
+        case 4: return reinterpret_cast<const void*>(rs_vec_edge<4, M, MODE>);
+        case 8: return reinterpret_cast<const void*>(rs_vec_edge<8, M, MODE>);
+        case 16: return reinterpret_cast<const void*>(rs_vec_edge<16, M, MODE>);
+        case 32: return reinterpret_cast<const void*>(rs_vec_edge<32, M, MODE>);
+        default: return nullptr;
+    }
+}
+
+template <int M, int MODE>
+const void* rs_kernel_for(int K, int W, bool edge) {
+    if (edge) return rs_edge_for<M, MODE>(K);
     return (W == 4) ? rs_vec_for<M, MODE, 4>(K) : rs_vec_for<M, MODE, 8>(K);
 }
 
@@ -250,8 +360,20 @@ const void* ar_vec_for(int K) {
     }
 }
 
+// The all-reduce's edge layout exists for K = 2, 4, 8 (edge_unit()).
 template <int MODE>
-const void* ar_kernel_for(int K, int W) {
+const void* ar_edge_for(int K) {
+    switch (K) {
+        case 2: return reinterpret_cast<const void*>(ar_vec_edge<2, MODE>);
+        case 4: return reinterpret_cast<const void*>(ar_vec_edge<4, MODE>);
+        case 8: return reinterpret_cast<const void*>(ar_vec_edge<8, MODE>);
+        default: return nullptr;
+    }
+}
+
+template <int MODE>
+const void* ar_kernel_for(int K, int W, bool edge) {
+    if (edge) return ar_edge_for<MODE>(K);
     return (W == 4) ? ar_vec_for<MODE, 4>(K) : ar_vec_for<MODE, 8>(K);
 }
 
@@ -262,12 +384,14 @@ cudaError_t launch_reduce_scatter(const RsParams& p, int mode, int width, cudaSt
     const void* k;
     dim3 grid;
     if (width > 0) {
+        const bool edge = p.edge != 0;
         if (mode == DPR_SUM_RING_FP32)
-            k = (p.M == 1) ? rs_kernel_for<1, DPR_SUM_RING_FP32>(p.K, width)
-                           : rs_kernel_for<2, DPR_SUM_RING_FP32>(p.K, width);
+            k = (p.M == 1) ? rs_kernel_for<1, DPR_SUM_RING_FP32>(p.K, width, edge)
+                           : rs_kernel_for<2, DPR_SUM_RING_FP32>(p.K, width, edge);
         else
-            k = (p.M == 1) ? rs_kernel_for<1, DPR_SUM_HOP_BF16>(p.K, width)
-                           : rs_kernel_for<2, DPR_SUM_HOP_BF16>(p.K, width);
+            k = (p.M == 1) ? rs_kernel_for<1, DPR_SUM_HOP_BF16>(p.K, width, edge)
+                           : rs_kernel_for<2, DPR_SUM_HOP_BF16>(p.K, width, edge);
+        if (!k) return cudaErrorInvalidDeviceFunction;   // an edge layout edge_unit() never sets
         grid = dim3(unsigned((uint64_t(p.su) + kThreads - 1) / kThreads), p.K);
     } else {
         k = (mode == DPR_SUM_RING_FP32) ? reinterpret_cast<const void*>(rs_scalar<DPR_SUM_RING_FP32>)
@@ -321,8 +445,9 @@ cudaError_t launch_allreduce(const ArParams& p, int mode, int width, cudaStream_
     const void* k;
     dim3 grid;
     if (width > 0) {
-        k = (mode == DPR_SUM_RING_FP32) ? ar_kernel_for<DPR_SUM_RING_FP32>(p.K, width)
-                                        : ar_kernel_for<DPR_SUM_HOP_BF16>(p.K, width);
+        k = (mode == DPR_SUM_RING_FP32) ? ar_kernel_for<DPR_SUM_RING_FP32>(p.K, width, p.edge != 0)
+                                        : ar_kernel_for<DPR_SUM_HOP_BF16>(p.K, width, p.edge != 0);
+        if (!k) return cudaErrorInvalidDeviceFunction;   // an edge layout edge_unit() never sets
         grid = dim3(unsigned((uint64_t(p.su) + kThreads - 1) / kThreads), p.K);
     } else {
         k = (mode == DPR_SUM_RING_FP32) ? reinterpret_cast<const void*>(ar_scalar<DPR_SUM_RING_FP32>)

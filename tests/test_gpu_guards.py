@@ -3,7 +3,9 @@
 All buffers of one call live in one device allocation, each behind a gap of
 guard bytes and at a chosen distance from 256-byte alignment, so that every
 layout runs: 32-byte vectors, 16-byte vectors and the element-wise kernels,
-with chunk lengths that leave ragged tails.  After the call, every byte outside
+with chunk lengths that leave ragged tails (the 32-byte kernels with an
+8-element edge unit per chunk need chunks of 2^22 elements and more; they
+have a test of their own below).  After the call, every byte outside
 the regions the call may write is compared with its value before the call:
 - the guard gaps (no write before or after a buffer);
 - the inputs (never written);
