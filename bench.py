@@ -1615,20 +1615,23 @@ def cpu_baseline(args):
     (the line's value) and the numpy simulation, with the numpy single-process
     figure beside them."""
     n = 1 << 20
-    smp, steps1, el1 = time_oracle(n, args.cpu_seconds / 3)
+    smp, steps1, el1 = time_oracle(n, args.cpu_seconds / 4)
     one = smp.bytes * steps1 / el1 / 1e9
     del smp
     cores = host_cores()
-    value, passes, el = time_pool(n, cores, "c", args.cpu_seconds / 3)
-    np_value, np_passes, np_el = time_pool(n, cores, "numpy", args.cpu_seconds / 3)
+    value, passes, el = time_pool(n, cores, "c", args.cpu_seconds / 4)
+    c_one, c_passes1, c_el1 = time_pool(n, 1, "c", args.cpu_seconds / 4)
+    np_value, np_passes, np_el = time_pool(n, cores, "numpy", args.cpu_seconds / 4)
     return {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
             "oracle": "C ring simulation (oracle/ring_sim.c, -O2, one thread per process)",
+            "single_core_value": round(c_one, 4),
             "numpy_value": round(np_value, 4), "numpy_single_core_value": round(one, 4),
             "sample": f"K=8, the same five steps; {cores} processes, each running the oracle "
                       f"on its own slab of {n} elements per rank (32 fragments of {n // 32}): "
                       f"C simulation {passes} passes in {el:.1f} s, numpy simulation "
-                      f"{np_passes} passes in {np_el:.1f} s; one numpy process alone: "
-                      f"{steps1} passes in {el1:.1f} s"}
+                      f"{np_passes} passes in {np_el:.1f} s; one process alone: C "
+                      f"{c_passes1} passes in {c_el1:.1f} s, numpy {steps1} passes in "
+                      f"{el1:.1f} s"}
 
 
 def common_config(world):
