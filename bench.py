@@ -883,8 +883,8 @@ def run_sequence_bench(args):
     """A backward pass's worth of small buckets issued back to back: 64
     buckets of 4 MiB per rank at K=8 (2 micro-batches, ring fp32, x1/8),
     reduce-scattered with plain launches, with programmatic dependent launches
-    (one call per bucket), and in one batched call; then the same 64 buckets
-    all-gathered with plain and programmatic launches and in one batched call.  Each figure is
+    (one call per bucket), as persistent requests and in one batched call;
+    then the same 64 buckets all-gathered the same four ways.  Each figure is
     the sequence's algorithmic bytes over its CUDA-event time, averaged over
     --steps sequences (4.8 GB per reduce-scatter sequence, far larger than
     L2, so no flush is needed).  The three reduce-scatter forms must give the
@@ -946,6 +946,12 @@ def run_sequence_bench(args):
         for b in range(nb):
             dpr.dpr_allgather(shards[b], K, N, full_l[b], stream=s)
 
+    ag_reqs = [dpr.dpr_allgather_init(shards[b], K, N, full_l[b]) for b in range(nb)]
+
+    def ag_requests():
+        for rq in ag_reqs:
+            rq.start(s)
+
     def ag_batch():
         dpr.dpr_allgather_batch(shards_all, K, [N] * nb, full, stream=s)
 
@@ -995,6 +1001,7 @@ def run_sequence_bench(args):
     t_rs_req = timed(rs_requests)
     t_rs_batch = timed(rs_batch)
     t_ag_pdl = timed(ag_single)
+    t_ag_req = timed(ag_requests)
     r, g = graphed(lambda: rs_single("pdl"))
     graphs.append(g)
     t_rs_pdl_g = timed(r)
@@ -1021,7 +1028,7 @@ def run_sequence_bench(args):
         "batched_call_us_per_bucket": round(host_us(rs_batch, nb), 2),
         "persistent_request_us_per_start": round(host_us(rs_requests, nb), 2),
     }
-    for rq in reqs:
+    for rq in reqs + ag_reqs:
         rq.close()
     peak, kind = load_peaks()
 
@@ -1047,6 +1054,7 @@ def run_sequence_bench(args):
                                "bytes": rs_bytes, "bit_identical": same},
             "allgather": {"plain_launches": fig(ag_bytes, t_ag_plain),
                           "programmatic_launches": fig(ag_bytes, t_ag_pdl),
+                          "persistent_requests": fig(ag_bytes, t_ag_req),
                           "one_batched_call": fig(ag_bytes, t_ag_batch),
                           "graph_plain_launches": fig(ag_bytes, t_ag_plain_g),
                           "graph_programmatic_launches": fig(ag_bytes, t_ag_pdl_g),
