@@ -1,13 +1,15 @@
 """GPU parity of the per-parameter (ZeRO-3 discrete path) reduce-scatter and
 all-gather against the CPU oracle, bit-exact: odd and empty parameters, zero
 padding, mixed alignments, both summation modes, accumulate, canaries around
-every written tensor, and config 3's 56 gradients at full size (sampled)."""
+every written tensor, and config 3's 56 gradients at full size (sampled against the numpy
+oracle, and at every element against the oracle's C ring simulation)."""
 import numpy as np
 import pytest
 import torch
 
 import gradient_reduction_gb300 as dpr
 from oracle import ring
+from oracle import ring_c
 from tests import gpu_helpers as H
 from workloads import configs as C
 from workloads import synthetic as syn
@@ -128,6 +130,17 @@ def test_cfg3_per_parameter_full_size(mode):
             idx = torch.from_numpy(o + T).to(dev)
             for j in range(K):
                 H.assert_f32_equal(out[j].index_select(0, idx).cpu().numpy(), want[j], f"p{p} j{j}")
+        # every element of every parameter's shards: the C ring simulation on each
+        # gradient copied back from the device and zero-padded to K * s
+        for p, (s, o, n) in enumerate(zip(sizes, offs, numel)):
+            x = []
+            for r in range(K):
+                a = np.zeros(K * s, dtype=np.uint16)
+                a[:n] = H.bits(grads[r][p].reshape(-1))
+                x.append(a)
+            want, _ = ring_c.reduce_scatter(x, K, 1, mode, 1.0 / K)
+            for j in range(K):
+                H.assert_f32_equal(out[j][o:o + s].cpu().numpy(), want[j], f"every p{p} j{j}")
         # the all-gather of the bf16-rounded partitions rebuilds every gradient's
         # all-reduce: compare parameter 2 (q) with dpr_allreduce of the same grads
         with dpr.dpr_coalesced_plan_create(
@@ -141,5 +154,12 @@ def test_cfg3_per_parameter_full_size(mode):
             for r in range(K):
                 assert torch.equal(agp._tensors[r * len(arr) + p].view(torch.int16),
                                    ar[r].view(torch.int16))
+            # and every parameter of every replica is its shards laid end to end,
+            # padding dropped
+            for q, (sq, oq, nq) in enumerate(zip(sizes, offs, numel)):
+                full = torch.cat([out[j][oq:oq + sq].to(torch.bfloat16) for j in range(K)])[:nq]
+                for r in range(K):
+                    got = agp._tensors[r * len(arr) + q].reshape(-1)
+                    assert torch.equal(got.view(torch.int16), full.view(torch.int16)), (q, r)
     del grads
     torch.cuda.empty_cache()
