@@ -1,12 +1,15 @@
 """GPU parity of the bf16 partition path (reduce-scatter into bf16 shards with
 copy_ / bf16 add_, and the step()-time cast) against the CPU oracle,
-bit-exact, plus config 2 at full size over two micro steps."""
+bit-exact, plus config 2 at full size over two micro steps (at every element
+against the oracle's C ring simulation)."""
 import numpy as np
 import pytest
 import torch
 
 import gradient_reduction_gb300 as dpr
+from oracle import bf16 as obf
 from oracle import ring
+from oracle import ring_c
 from tests import gpu_helpers as H
 from tests.test_gpu_collectives import _inputs, _upload
 from workloads import configs as C
@@ -62,8 +65,9 @@ def test_cast_parity(n, offset):
 def test_cfg2_two_micro_steps_then_cast(mode):
     """Config 2 (K=8, 25 M elements): micro step 0 copies the shard into the
     bf16 partition, micro step 1 adds the next micro-batch's shard in bf16,
-    step() casts to fp32.  Sampled oracle check; over every element the copy
-    equals bf16 of the fp32 reduce-scatter."""
+    step() casts to fp32.  Sampled numpy-oracle check, and every element
+    against the C ring simulation; over every element the copy also equals
+    bf16 of the fp32 reduce-scatter."""
     dev = H.device()
     cfg = C.CFG2
     K, N = cfg.K, cfg.N
@@ -92,3 +96,12 @@ def test_cfg2_two_micro_steps_then_cast(mode):
         H.assert_bf16_equal(H.bits(part[j].index_select(0, idx)), p1[j], f"shard {j}")
         assert np.array_equal(cast[j].index_select(0, idx).cpu().numpy().view(np.uint32),
                               ring.cast_partition(p1[j]).view(np.uint32))
+    # every element: the C ring simulation's fp32 shards of both micro steps,
+    # rounded to bf16 and added in bf16 (copy_, then add_), then widened
+    s0, _ = ring_c.reduce_scatter([H.bits(t) for t in x0], K, 1, mode, 1.0 / K)
+    s1, _ = ring_c.reduce_scatter([H.bits(t) for t in x1], K, 1, mode, 1.0 / K)
+    for j in range(K):
+        want = obf.add(obf.from_f32(s0[j]), obf.from_f32(s1[j]))
+        H.assert_bf16_equal(H.bits(part[j]), want, f"every shard {j}")
+        assert np.array_equal(cast[j].cpu().numpy().view(np.uint32),
+                              obf.to_f32(want).view(np.uint32)), j

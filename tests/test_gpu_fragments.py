@@ -124,8 +124,10 @@ def test_reduce_scatter_fragments_guards():
 
 def test_cfg3_fragments_full_size():
     """Configuration 3's 42 buckets: each bucket reduced straight from its
-    gradients equals the gather + reduce-scatter of that bucket, bit for bit;
-    three buckets are also checked against the oracle at sampled positions."""
+    gradients equals the gather + reduce-scatter of that bucket, bit for bit,
+    and the oracle's C ring simulation on the gathered bucket at every element;
+    three buckets are also checked against the numpy oracle at sampled
+    positions."""
     dev = H.device()
     cfg = C.CFG3
     K = cfg.K
@@ -156,6 +158,8 @@ def test_cfg3_fragments_full_size():
             torch.cuda.synchronize()
         for j in range(K):
             assert torch.equal(out[j].view(torch.int32), ref[j].view(torch.int32)), (bi, j)
+        # every element, against the C ring simulation on the gathered bucket
+        H.assert_rs_every_element(views, out, K, 1, ring.RING_FP32, 1.0 / K, f"bucket {bi}")
         if bi in (0, 17, 41):
             T = H.sample_positions(S, 32, bi)
             idx = H.chunk_positions(K, S, T)
