@@ -34,5 +34,5 @@ def add(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
     to bf16 (the fp32 sum of two bf16 values is exact unless their exponents
     differ by more than 15, and then the smaller one is too small to move the
     bf16 rounding, so this is the correctly rounded bf16 sum)."""
-    with np.errstate(over="ignore"):
+    with np.errstate(over="ignore", invalid="ignore"):     # inf + -inf is NaN, as in IEEE
         return from_f32(to_f32(a_bits) + to_f32(b_bits))
