@@ -8,8 +8,8 @@ chunks keep 16-byte accesses and are covered by the other parity tests, as is
 the in-place all-reduce here, which keeps them at any length.
 
 Every element is compared with the oracle's C ring simulation (bit-exact, NaN
-as NaN): both summation modes, one and two micro-batches, copy and
-accumulate; a guard test checks that no byte outside the written regions
+as NaN), for every K, micro-batch count and summation mode the edge kernels
+are built for, copy and accumulate; a guard test checks that no byte outside the written regions
 changes, so the window's reads of the neighbouring chunk leave no trace."""
 import pytest
 import torch
@@ -35,8 +35,10 @@ def _x_dev(K, M, N, seed, dev):
     return xd, [H.bits(t) for t in xd]
 
 
+# every (K, M) the reduce-scatter's edge kernels are built for, both modes below
 RS_EDGE = [(2, S_EDGE, 1), (2, S_EDGE_LONG, 2), (4, S_EDGE_LONG, 1), (4, S_EDGE, 2),
-           (8, S_EDGE, 1), (8, S_EDGE_LONG, 2), (16, S_EDGE, 1)]
+           (8, S_EDGE, 1), (8, S_EDGE_LONG, 2), (16, S_EDGE, 1), (16, S_EDGE, 2),
+           (32, S_EDGE, 1), (32, S_EDGE, 2)]
 
 
 @pytest.mark.parametrize("K,S,M", RS_EDGE)
