@@ -70,29 +70,29 @@ BF16_KERNELS = ("rs_bf16_copy", "rs_bf16_add", "cast")
 # underestimate.
 NCU_TRAFFIC = {
     "flatten": {"bytes": 16_290_209_792, "small_case_bytes": 1_018_138_112, "scale": 16,
-        "src_sha": "578139312553fd43"},
+        "src_sha": "b613c2b04ba85972"},
     "rs_fp32_m2": {"bytes": 19_163_496_448, "small_case_bytes": 1_197_718_528, "scale": 16,
-        "src_sha": "bf44fabf80dea9cc"},
+        "src_sha": "9d0af4a9c5c06563"},
     "rs_hop_m2_acc": {"bytes": 21_305_192_448, "small_case_bytes": 1_331_574_528, "scale": 16,
-        "src_sha": "bf44fabf80dea9cc"},
+        "src_sha": "9d0af4a9c5c06563"},
     "allgather": {"bytes": 8_736_522_240, "small_case_bytes": 546_032_640, "scale": 16,
-        "src_sha": "578139312553fd43"},
+        "src_sha": "b613c2b04ba85972"},
     "allreduce": {"bytes": 16_272_740_352, "small_case_bytes": 1_017_046_272, "scale": 16,
-        "src_sha": "bf44fabf80dea9cc"},
+        "src_sha": "9d0af4a9c5c06563"},
     "rs_fp32_m1": {"bytes": 10_433_806_336, "small_case_bytes": 652_112_896, "scale": 16,
-        "src_sha": "bf44fabf80dea9cc"},
+        "src_sha": "9d0af4a9c5c06563"},
     "rs_hop_m1": {"bytes": 10_429_546_496, "small_case_bytes": 651_846_656, "scale": 16,
-        "src_sha": "bf44fabf80dea9cc"},
+        "src_sha": "9d0af4a9c5c06563"},
     "rs_coalesced": {"bytes": 21_887_973_632, "small_case_bytes": 3_126_853_376, "scale": 7,
-        "src_sha": "73cc97b61fdb9af0"},
+        "src_sha": "6db8cec815e4b3a0"},
     "ag_coalesced": {"bytes": 19_398_374_912, "small_case_bytes": 2_771_196_416, "scale": 7,
-        "src_sha": "5938d73fd6467d76"},
+        "src_sha": "9fdeaea1861c48c0"},
     "rs_bf16_copy": {"bytes": 9_522_950_144, "small_case_bytes": 595_184_384, "scale": 16,
-        "src_sha": "bf44fabf80dea9cc"},
+        "src_sha": "9d0af4a9c5c06563"},
     "rs_bf16_add": {"bytes": 10_583_232_512, "small_case_bytes": 661_452_032, "scale": 16,
-        "src_sha": "bf44fabf80dea9cc"},
+        "src_sha": "9d0af4a9c5c06563"},
     "cast": {"bytes": 2_331_922_432, "small_case_bytes": 145_745_152, "scale": 16,
-        "src_sha": "f16c6d4024820bfc"},
+        "src_sha": "be25e80a1cc2945b"},
 }
 
 

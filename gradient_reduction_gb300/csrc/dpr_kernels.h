@@ -109,7 +109,8 @@ inline int access_width(int64_t S, bool aligned32, bool aligned16) {
 // 2.1M (shorter launches gain from the 16-byte kernel's finer blocks), so
 // shorter chunks keep 16-byte accesses.
 // The layout is built for the reduce-scatter at K = 2, 4, 8, 16, 32 and the
-// all-reduce at K = 2, 4, 8: there it fits 64 registers without spilling.
+// all-reduce at K = 2, 4, 8: there it fits 64 registers, spilling at most 4
+// bytes (the fp32 reduce-scatter at K = 16 and 32).
 constexpr int64_t kEdgeMinChunk = int64_t(1) << 22;
 inline bool edge_unit(int64_t S, int K, bool aligned32, bool allreduce) {
     const bool built = allreduce ? (K == 2 || K == 4 || K == 8)

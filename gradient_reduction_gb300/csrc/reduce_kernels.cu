@@ -42,7 +42,8 @@ namespace {
 // an even chunk has one after it); the inputs are read-only here, those 8
 // sums are dropped and only the chunk's own 8 are stored.  The edge unit thus
 // runs the same 32-byte code as every other unit.  The kernel is capped at 64
-// registers (4 blocks per SM); for the K it is built for it does not spill.
+// registers (4 blocks per SM); for the K it is built for it spills at most 4
+// bytes.
 template <int KC, int M, int MODE, int W, bool EDGE>
 __device__ __forceinline__ void rs_units(const RsParams& p) {
     static_assert(!EDGE || W == 8, "the edge layout has 32-byte units");
