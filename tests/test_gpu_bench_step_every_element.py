@@ -1,6 +1,8 @@
 """One step of the bench workload at its full size (K = 8, 1 GiB per rank,
 N = 2**29), with every element of both reduce-scatters and of the all-reduce
-compared against the oracle, bit for bit (a NaN matches any NaN).
+compared against the oracle, bit for bit (a NaN matches any NaN); and the
+metric's own reduce-scatter (one micro-batch, both modes) at the same size
+against the oracle's C ring simulation.
 
 The inputs the oracle consumes are the generator's: the bucket's fragments,
 the second micro-batch and the partitions the hop-mode reduce-scatter
@@ -23,6 +25,7 @@ import torch
 
 from oracle import flatten as ofl
 from oracle import ring
+from oracle import ring_c
 from tests import gpu_helpers as H
 from workloads import configs as C
 
@@ -94,3 +97,38 @@ def test_bench_step_every_element():
     with cf.ThreadPoolExecutor(max_workers=workers) as ex:
         done = sum(ex.map(check, range(0, S, SLAB)))
     assert done == S
+
+
+def test_metric_reduce_scatter_every_element():
+    """The metric's own operation at its full size -- the reduce-scatter of one
+    micro-batch, K = 8, 1 GiB per rank, in both summation modes, launched as
+    the bench launches it -- at every element against the oracle's C ring
+    simulation, slab by slab."""
+    dev = H.device()
+    import bench
+    torch.cuda.empty_cache()
+    w = C.BENCH
+    K, N = w.K, w.N
+    S = N // K
+    stream = torch.cuda.Stream()
+    wl = bench.Workload(dev, stream)
+    ipg0 = _host(wl.ipg0_all.view(torch.int16)).view(np.uint16)
+    got = {}
+    for name in ("rs_fp32_m1", "rs_hop_m1"):
+        wl.launch(name)
+        stream.synchronize()
+        got[name] = _host(wl.part_f32_all)
+    wl.plan.close()
+    del wl
+    torch.cuda.empty_cache()
+
+    def sub(bufs, t0, t1):
+        return [np.concatenate([b[c * S + t0:c * S + t1] for c in range(K)]) for b in bufs]
+
+    for t0 in range(0, S, SLAB):
+        t1 = min(S, t0 + SLAB)
+        x = sub(list(ipg0), t0, t1)
+        for name, mode in (("rs_fp32_m1", ring_c.RING_FP32), ("rs_hop_m1", ring_c.HOP_BF16)):
+            want, _ = ring_c.reduce_scatter(x, K, 1, mode, 1.0 / K)
+            for j in range(K):
+                H.assert_f32_equal(got[name][j][t0:t1], want[j], f"{name} shard {j} at {t0}")
