@@ -3,7 +3,7 @@ infrastructure).
 
 The C simulation restates the same rounds as `oracle.ring` (see the C file's
 header for the pages it follows) in plain C, so that the host's cores run it
-at memory speed: the bench's CPU baseline times it, and the tests check it
+faster than numpy: the bench's CPU baseline times it, and the tests check it
 against its own pins and against the numpy simulation.  Results use the same
 representation as `oracle.ring`: uint16 arrays of bf16 bits, float32 arrays
 for fp32 partitions.

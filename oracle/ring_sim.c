@@ -2,7 +2,7 @@
  * Ring simulation in plain C -- ORACLE, TEST INFRASTRUCTURE.
  *
  * A second CPU statement of what the ZeRO gradient-bucket reduction computes,
- * written in C so that the host's cores can run it at memory speed.  Like the
+ * written in C so that the host's cores run it faster than numpy.  Like the
  * numpy oracle beside it, it follows the pages round by round and shares no
  * code with the CUDA library; only the test suite, the package smoke check and
  * the bench's CPU legs load it.
